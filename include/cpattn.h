@@ -1,0 +1,232 @@
+/*
+ * cpattn -- context-parallel ring attention for one GB300 (sm_103a).
+ *
+ * The C ABI of the hot path behind context parallelism (CP): blockwise causal
+ * ring attention over a packed variable-length (THD) batch, with the
+ * online-softmax merge that folds each KV chunk's partial result into the
+ * running (O, m, l), and the dynamic-CP planner that picks each sample's CP
+ * size.  CP is emulated on one GPU: a sample split over c ranks becomes c
+ * chunks resident in device memory, and the ring's KV hand-off becomes a loop
+ * over those chunks in ring order.
+ *
+ * Sources (cited by title and section):
+ *   [6D-CP] "Megatron 架构与 6D 并行完整指南", section 六 (context parallelism in
+ *           depth): the ring_attention listing and its online-softmax merge.
+ *   [DCP]   "Dynamic Context Parallelism (DCP)", verl 0.9.0 docs,
+ *           docs/advance/dynamic_context_parallel.
+ *   [MCore] "20-Megatron-MCore-TP-PP-EP如何支撑MoE", sections 1 and 4.
+ *
+ * Conventions shared by every call:
+ *   - Packed THD layout.  Q, K, V and O are [T, H, D] row-major (D fastest);
+ *     LSE, m and l are [T, H]; per-step partials are [S, T, H, D] and
+ *     [S, T, H].  cu_seqlens is the [B + 1] prefix sum of sample lengths,
+ *     cu_seqlens[0] = 0 and cu_seqlens[B] = T.
+ *   - Positions are 0-based within a sample.  A sample of length L with CP
+ *     size c is split into contiguous chunks of ceil(L / c) tokens; chunk r is
+ *     [r * ceil(L/c), min((r+1) * ceil(L/c), L)) and the last chunks may be
+ *     short or empty.  Rank r holds Q chunk r and, at ring step s, the KV chunk
+ *     of rank (r - s) mod c.
+ *   - Causal attention lets position p see key positions 0..p of its own
+ *     sample.  Scores are softmax_scale * <q, k>; LSE is the natural-log
+ *     log-sum-exp of the scaled scores.
+ *   - The library allocates no device memory.  Every buffer is owned by the
+ *     caller; the library never frees or retains one past the call (except
+ *     through work already enqueued on `stream`).
+ *   - Device calls enqueue on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and return without synchronising.  Argument errors are detected
+ *     on the host and return before anything is enqueued.  Errors found by the
+ *     kernels (bad cu_seqlens, a CP size above max_cp, a bounded wait that ran
+ *     out) are written to the workspace's error word and read back with
+ *     cpattn_poll_error.
+ *   - Device pointers must be 16-byte aligned; float arrays 4-byte aligned.
+ *   - Thread safety: calls may be made from several host threads; internal
+ *     state is a mutex-guarded cache of device properties.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = 1,        /* bad pointer, size, alignment or layout   */
+  CPATTN_ERR_UNSUPPORTED = 2,        /* e.g. head_dim other than 64 or 128       */
+  CPATTN_ERR_WORKSPACE_TOO_SMALL = 3,
+  CPATTN_ERR_PLAN_INFEASIBLE = 4,    /* a sample does not fit at max_cp          */
+  CPATTN_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed        */
+  CPATTN_ERR_DEVICE_TIMEOUT = 6      /* a kernel's bounded wait ran out          */
+} cpattn_status;
+
+/* Kernel modes of cpattn_fwd. */
+#define CPATTN_MODE_FUSED 0    /* merge folded into the attention kernel        */
+#define CPATTN_MODE_UNFUSED 1  /* per-step partials in the workspace, then merge */
+
+/*
+ * cpattn_plan -- dynamic-CP planning of one mini-batch (host only).
+ *
+ * [DCP]: the CP size is chosen per sample from its length by a
+ * sequence-length-aware scheduler; every DPxCP rank sees the same samples;
+ * the DPxCP world size is even and at least 2; CP groups are power-of-two
+ * subgroups plus, when needed, the full DPxCP group; the per-rank packing
+ * limit is max_seqlen_per_dp_cp_rank (the static budget divided by the static
+ * CP size, e.g. 16384 / 4 = 4096).  [MCore] section 4: a micro-batch holds
+ * world * limit tokens.  The pages do not give the scheduler's algorithm;
+ * this call implements the following deterministic rules:
+ *   1. cp_size[b] = smallest c in {1, 2, 4, ... < max_cp} U {max_cp} with
+ *      ceil(seqlens[b] / c) <= max_seqlen_per_dp_cp_rank;
+ *   2. samples are placed longest first, equal lengths by ascending index;
+ *   3. a sample with CP c occupies an aligned rank group [g*c, (g+1)*c),
+ *      g = 0 .. world/c - 1, adding ceil(L / c) tokens to each rank's load;
+ *   4. first fit: the first micro-batch (in creation order) and within it the
+ *      first group where every rank stays within the limit; otherwise a new
+ *      micro-batch is opened and the sample takes its group 0.
+ *
+ * Arguments (all host memory, owned by the caller):
+ *   seqlens            [n] sample lengths, each >= 0.
+ *   n                  number of samples, >= 0.
+ *   dpxcp_world_size   W, even, 2 <= W <= 4096.
+ *   max_seqlen_per_dp_cp_rank   per-rank token limit, >= 1.
+ *   max_cp             largest CP size: a power of two <= W, or W itself.
+ *   cp_size, micro_batch, first_rank   [n] outputs per original sample index.
+ *   order              [n] output: sample indices in placement order.
+ *   num_micro_batches  [1] output.
+ *   rank_load          [n * W] output or NULL: rank_load[mb * W + r] is the
+ *                      token load of rank r in micro-batch mb, for
+ *                      mb < *num_micro_batches; the rest is left untouched.
+ * Returns CPATTN_OK, CPATTN_ERR_INVALID_ARG (argument rule broken; outputs
+ * untouched) or CPATTN_ERR_PLAN_INFEASIBLE (some ceil(L / max_cp) exceeds the
+ * limit; outputs untouched).
+ */
+int cpattn_plan(const int32_t* seqlens, int32_t n, int32_t dpxcp_world_size,
+                int32_t max_seqlen_per_dp_cp_rank, int32_t max_cp,
+                int32_t* cp_size, int32_t* micro_batch, int32_t* first_rank,
+                int32_t* order, int32_t* num_micro_batches, int32_t* rank_load);
+
+/*
+ * cpattn_fwd_workspace_size -- bytes of device workspace cpattn_fwd needs.
+ *
+ * total_tokens T, num_seqs B, num_heads H, head_dim D, max_cp (the bound on
+ * every cp_size[b]) and mode as passed to cpattn_fwd.  In CPATTN_MODE_UNFUSED
+ * the workspace also holds the per-step partials (max_cp * T * H * (D + 2)
+ * floats).  Returns 0 for invalid arguments.
+ */
+size_t cpattn_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t max_cp, int32_t mode);
+
+/*
+ * cpattn_fwd -- ring attention forward over a packed THD batch.
+ *
+ * [6D-CP] ring_attention: for every sample b split into c = cp_size[b]
+ * chunks and every rank i, start from O = 0, m = -inf, l = 0; for
+ * step = 0 .. c-1 attend Q chunk i to KV chunk (i - step) mod c (block
+ * attention giving O_step, m_step, l_step) and fold it in with
+ *   m_new = max(m, m_step), alpha = exp(m - m_new), beta = exp(m_step - m_new),
+ *   l = alpha * l + beta * l_step, O = alpha * O + beta * O_step, m = m_new;
+ * return O / l.  The result equals full softmax attention of each sample up
+ * to rounding.  CPATTN_MODE_FUSED keeps (O, m, l) on chip for all steps;
+ * CPATTN_MODE_UNFUSED writes every step's (O_step, m_step, l_step) to the
+ * workspace and folds them with the merge kernel.
+ *
+ * Arguments:
+ *   q, k, v        device, bf16 [T, H, D], 16-byte aligned.
+ *   cu_seqlens     device int32 [B + 1].
+ *   cp_size        device int32 [B] with 1 <= cp_size[b] <= max_cp, or NULL
+ *                  (every sample at CP 1).
+ *   num_seqs       B >= 0.   total_tokens  T >= 0 (= cu_seqlens[B]).
+ *   max_seqlen     upper bound on every sample length (> 0 when T > 0).
+ *   max_cp         upper bound on cp_size[b], 1 .. 64.
+ *   num_heads      H >= 1.   head_dim  D in {64, 128} (else UNSUPPORTED).
+ *   softmax_scale  multiplies <q, k>; finite and > 0.
+ *   causal         1 causal, 0 full attention within each sample.
+ *   mode           CPATTN_MODE_FUSED or CPATTN_MODE_UNFUSED.
+ *   out            device bf16 [T, H, D]: O / l.
+ *   lse            device float [T, H]: m + ln l (natural log).  May be NULL.
+ *   workspace      device, >= cpattn_fwd_workspace_size(...) bytes, 256-byte
+ *                  aligned; its first bytes hold the error word.
+ *   stream         cudaStream_t.
+ * The kernels check cu_seqlens (non-decreasing, cu[0] = 0, cu[B] = T, every
+ * length <= max_seqlen) and cp_size (1 .. max_cp); a violation sets
+ * CPATTN_ERR_INVALID_ARG in the error word and writes no output.
+ */
+int cpattn_fwd(const void* q, const void* k, const void* v,
+               const int32_t* cu_seqlens, const int32_t* cp_size,
+               int32_t num_seqs, int64_t total_tokens, int32_t max_seqlen,
+               int32_t max_cp, int32_t num_heads, int32_t head_dim,
+               float softmax_scale, int32_t causal, int32_t mode,
+               void* out, float* lse, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/*
+ * cpattn_fwd_partials -- the per-step block attentions of the ring, stored.
+ *
+ * [6D-CP]: the result of each ring step's block attention before it is
+ * merged: for token t (rank i of its sample) and step s < c,
+ *   m_steps[s, t, h] = max of the visible scaled scores against KV chunk
+ *                      (i - s) mod c (-inf when none is visible),
+ *   l_steps[s, t, h] = sum of exp(score - m_steps),
+ *   o_steps[s, t, h, :] = sum of exp(score - m_steps) * v  (not normalised).
+ * Steps s >= c, and steps that see no key, hold (0, -inf, 0).  The kernel may
+ * use any reference value in place of the exact step maximum, as long as
+ * o_steps and l_steps are scaled by the same exp(-reference): every quantity
+ * the merge uses (O_step / l_step and m_step + ln l_step) is unchanged.
+ *
+ * Arguments as cpattn_fwd, plus:
+ *   num_steps  S >= max_cp.
+ *   o_steps    device float [S, T, H, D];  m_steps, l_steps device float
+ *              [S, T, H].  Caller-owned; every element is written.
+ *   workspace  >= cpattn_fwd_workspace_size(T, B, H, D, max_cp,
+ *              CPATTN_MODE_FUSED) bytes.
+ */
+int cpattn_fwd_partials(const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens, const int32_t* cp_size,
+                        int32_t num_seqs, int64_t total_tokens,
+                        int32_t max_seqlen, int32_t max_cp, int32_t num_heads,
+                        int32_t head_dim, float softmax_scale, int32_t causal,
+                        int32_t num_steps, float* o_steps, float* m_steps,
+                        float* l_steps, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * cpattn_merge -- fold S stored partials with the [6D-CP] merge.
+ *
+ * For every row (t, h): starting from (O, m, l) = (0, -inf, 0), fold steps
+ * s = 0 .. S-1 with the formulas above; exp(-inf - x) counts as 0.  Writes
+ *   out_o[t, h, :] = O / l (0 when l = 0), out_m[t, h] = m, out_l[t, h] = l.
+ * The kernel evaluates the fold in closed form (m* = max_s m_s first, then
+ * sums weighted by exp(m_s - m*)), which is the same value up to rounding.
+ *
+ * Arguments (device float, caller-owned, 16-byte aligned):
+ *   o_steps [S, T, H, D], m_steps [S, T, H], l_steps [S, T, H];
+ *   num_steps S in 1 .. 64; T >= 0; H >= 1; D in {64, 128};
+ *   out_o [T, H, D]; out_m, out_l [T, H] (either may be NULL).
+ */
+int cpattn_merge(const float* o_steps, const float* m_steps,
+                 const float* l_steps, int32_t num_steps, int64_t total_tokens,
+                 int32_t num_heads, int32_t head_dim, float* out_o,
+                 float* out_m, float* out_l, void* stream);
+
+/*
+ * cpattn_poll_error -- synchronise `stream` and return the workspace's error
+ * word (CPATTN_OK when every kernel since the last cpattn_fwd on this
+ * workspace finished normally), or CPATTN_ERR_CUDA if the stream reports a
+ * CUDA error.  The word is cleared by the next cpattn_fwd on the workspace.
+ */
+int cpattn_poll_error(const void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* cpattn_status_string(int status);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int cpattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

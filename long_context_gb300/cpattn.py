@@ -1,0 +1,263 @@
+"""Python binding of the cpattn C ABI (``include/cpattn.h``).
+
+Argument marshalling only: tensors are checked for dtype, device, layout and
+contiguity, then their device pointers are handed to ``libcpattn.so`` together
+with PyTorch's current CUDA stream.  Every step of the computation runs in the
+library's kernels; there is no fallback.  Importing this module raises
+``ImportError`` when the library has not been built (``build.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcpattn.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        "libcpattn.so is missing at %s; build it with "
+        "long_context_gb300.build.build()" % _LIB_PATH)
+_lib = ctypes.CDLL(_LIB_PATH)
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE_TOO_SMALL = 3
+ERR_PLAN_INFEASIBLE = 4
+ERR_CUDA = 5
+ERR_DEVICE_TIMEOUT = 6
+MODE_FUSED = 0
+MODE_UNFUSED = 1
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+
+_lib.cpattn_plan.argtypes = [_i32p, _i32, _i32, _i32, _i32, _i32p, _i32p, _i32p,
+                             _i32p, _i32p, _i32p]
+_lib.cpattn_plan.restype = ctypes.c_int
+_lib.cpattn_fwd_workspace_size.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32]
+_lib.cpattn_fwd_workspace_size.restype = ctypes.c_size_t
+_lib.cpattn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                            _i32, ctypes.c_float, _i32, _i32, _vp, _vp, _vp,
+                            ctypes.c_size_t, _vp]
+_lib.cpattn_fwd.restype = ctypes.c_int
+_lib.cpattn_fwd_partials.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                     _i32, _i32, ctypes.c_float, _i32, _i32, _vp, _vp,
+                                     _vp, _vp, ctypes.c_size_t, _vp]
+_lib.cpattn_fwd_partials.restype = ctypes.c_int
+_lib.cpattn_merge.argtypes = [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
+_lib.cpattn_merge.restype = ctypes.c_int
+_lib.cpattn_poll_error.argtypes = [_vp, _vp]
+_lib.cpattn_poll_error.restype = ctypes.c_int
+_lib.cpattn_status_string.argtypes = [ctypes.c_int]
+_lib.cpattn_status_string.restype = ctypes.c_char_p
+_lib.cpattn_version.argtypes = []
+_lib.cpattn_version.restype = ctypes.c_int
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+def status_string(status):
+    return _lib.cpattn_status_string(int(status)).decode()
+
+
+def version():
+    v = _lib.cpattn_version()
+    return (v >> 16, (v >> 8) & 0xFF, v & 0xFF)
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def _check(status, what):
+    if status != OK:
+        raise CpattnError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (name, device, t.device))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+# ---------------------------------------------------------------- planner --
+
+def plan(seqlens, dpxcp_world_size, max_seqlen_per_dp_cp_rank, max_cp):
+    """``cpattn_plan`` on host arrays; returns a dict of NumPy int32 arrays.
+
+    Keys: ``cp_size``, ``micro_batch``, ``first_rank``, ``order`` (length n),
+    ``num_micro_batches`` (int) and ``rank_load`` ([num_micro_batches, W]).
+    Raises :class:`CpattnError` on invalid arguments or an infeasible plan.
+    """
+    lens = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    n = int(lens.shape[0])
+    W = int(dpxcp_world_size)
+    outs = [np.zeros(max(n, 1), dtype=np.int32) for _ in range(4)]
+    nmb = np.zeros(1, dtype=np.int32)
+    load = np.zeros(max(n * W, 1) if W > 0 else 1, dtype=np.int32)
+    p = lambda a: a.ctypes.data_as(_i32p)  # noqa: E731
+    st = _lib.cpattn_plan(p(lens) if n else None, n, W, int(max_seqlen_per_dp_cp_rank),
+                          int(max_cp), p(outs[0]), p(outs[1]), p(outs[2]), p(outs[3]),
+                          p(nmb), p(load))
+    _check(st, "cpattn_plan")
+    k = int(nmb[0])
+    return {
+        "cp_size": outs[0][:n].copy(),
+        "micro_batch": outs[1][:n].copy(),
+        "first_rank": outs[2][:n].copy(),
+        "order": outs[3][:n].copy(),
+        "num_micro_batches": k,
+        "rank_load": load[:k * W].reshape(k, W).copy(),
+    }
+
+
+# ---------------------------------------------------------------- forward --
+
+def workspace_size(total_tokens, num_seqs, num_heads, head_dim, max_cp, mode=MODE_FUSED):
+    n = _lib.cpattn_fwd_workspace_size(int(total_tokens), int(num_seqs), int(num_heads),
+                                       int(head_dim), int(max_cp), int(mode))
+    if n == 0:
+        raise CpattnError(ERR_INVALID_ARG, "cpattn_fwd_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(total_tokens, num_seqs, num_heads, head_dim, max_cp, mode=MODE_FUSED,
+                    device=None):
+    """A device workspace sized for the given problem (torch-owned)."""
+    n = workspace_size(total_tokens, num_seqs, num_heads, head_dim, max_cp, mode)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _fwd_common(q, k, v, cu_seqlens, cp_size):
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, D]")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q, k, v must be CUDA tensors")
+    _need(k, "k", torch.bfloat16, dev, q.shape)
+    _need(v, "v", torch.bfloat16, dev, q.shape)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if cp_size is not None:
+        _need(cp_size, "cp_size", torch.int32, dev, (cu_seqlens.numel() - 1,))
+    return dev
+
+
+def fwd(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None, softmax_scale=None,
+        causal=True, mode=MODE_FUSED, out=None, lse=None, workspace=None, stream=None):
+    """Ring-attention forward (``cpattn_fwd``); returns ``(out, lse)``.
+
+    ``q, k, v``: bf16 ``[T, H, D]``; ``cu_seqlens``: int32 ``[B + 1]``;
+    ``cp_size``: int32 ``[B]`` or None (CP 1 everywhere), all on the GPU.
+    ``max_seqlen`` and ``max_cp`` bound the sample lengths and CP sizes.
+    """
+    dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    if max_cp is None:
+        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, dev, q.shape)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    else:
+        _need(lse, "lse", torch.float32, dev, (T, H))
+    if workspace is None:
+        workspace = alloc_workspace(T, B, H, D, max_cp, mode, dev)
+    st = _lib.cpattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cp_size), B, T,
+                         int(max_seqlen), int(max_cp), H, D, float(softmax_scale),
+                         1 if causal else 0, int(mode), _ptr(out), _ptr(lse),
+                         _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "cpattn_fwd")
+    return out, lse
+
+
+def fwd_partials(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp, num_steps=None,
+                 softmax_scale=None, causal=True, o_steps=None, m_steps=None, l_steps=None,
+                 workspace=None, stream=None):
+    """Per-ring-step partials (``cpattn_fwd_partials``); returns ``(o, m, l)``."""
+    dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    S = int(num_steps or max_cp)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if o_steps is None:
+        o_steps = torch.empty((S, T, H, D), dtype=torch.float32, device=dev)
+    if m_steps is None:
+        m_steps = torch.empty((S, T, H), dtype=torch.float32, device=dev)
+    if l_steps is None:
+        l_steps = torch.empty((S, T, H), dtype=torch.float32, device=dev)
+    _need(o_steps, "o_steps", torch.float32, dev, (S, T, H, D))
+    _need(m_steps, "m_steps", torch.float32, dev, (S, T, H))
+    _need(l_steps, "l_steps", torch.float32, dev, (S, T, H))
+    if workspace is None:
+        workspace = alloc_workspace(T, B, H, D, max_cp, MODE_FUSED, dev)
+    st = _lib.cpattn_fwd_partials(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cp_size),
+                                  B, T, int(max_seqlen), int(max_cp), H, D,
+                                  float(softmax_scale), 1 if causal else 0, S, _ptr(o_steps),
+                                  _ptr(m_steps), _ptr(l_steps), _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check(st, "cpattn_fwd_partials")
+    return o_steps, m_steps, l_steps
+
+
+def merge(o_steps, m_steps, l_steps, *, out_o=None, out_m=None, out_l=None, stream=None):
+    """Fold stored partials (``cpattn_merge``); returns ``(O / l, m, l)`` in fp32."""
+    _need(o_steps, "o_steps", torch.float32)
+    if o_steps.dim() != 4 or o_steps.device.type != "cuda":
+        raise ValueError("o_steps must be a CUDA [S, T, H, D] tensor")
+    S, T, H, D = o_steps.shape
+    dev = o_steps.device
+    _need(m_steps, "m_steps", torch.float32, dev, (S, T, H))
+    _need(l_steps, "l_steps", torch.float32, dev, (S, T, H))
+    if out_o is None:
+        out_o = torch.empty((T, H, D), dtype=torch.float32, device=dev)
+    if out_m is None:
+        out_m = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if out_l is None:
+        out_l = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out_o, "out_o", torch.float32, dev, (T, H, D))
+    _need(out_m, "out_m", torch.float32, dev, (T, H))
+    _need(out_l, "out_l", torch.float32, dev, (T, H))
+    st = _lib.cpattn_merge(_ptr(o_steps), _ptr(m_steps), _ptr(l_steps), S, T, H, D,
+                           _ptr(out_o), _ptr(out_m), _ptr(out_l), _stream(stream))
+    _check(st, "cpattn_merge")
+    return out_o, out_m, out_l
+
+
+def poll_error(workspace, stream=None):
+    """Synchronise the stream and return the workspace's error word."""
+    return int(_lib.cpattn_poll_error(_ptr(workspace), _stream(stream)))

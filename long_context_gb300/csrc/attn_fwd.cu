@@ -1,0 +1,552 @@
+// Ring-attention forward for sm_103a: block attention on the tensor cores
+// (tcgen05, accumulators in TMEM, Q/K/V tiles staged by TMA) with the
+// online-softmax merge of the ring folded into the same kernel.
+//
+// What is computed follows the ring_attention listing of "Megatron 架构与 6D
+// 并行完整指南", section 六: a sample split into c CP chunks; rank i holds Q chunk
+// i and at ring step s the KV chunk (i - s) mod c; each step's block attention
+// (O_step, m_step, l_step) is folded into (O, m, l) with
+//   m_new = max(m, m_step), alpha = exp(m - m_new), beta = exp(m_step - m_new),
+//   l = alpha l + beta l_step, O = alpha O + beta O_step,
+// and the result is O / l.  The kernel walks the same chunks in the same ring
+// order, 128 keys at a time, and applies that merge after every KV tile
+// rather than only at chunk boundaries (a KV tile is a sub-block of a chunk,
+// so the fold is the same operation at a finer grain).  In partials mode the
+// running state restarts at every ring step and each step's (O_step, m_step,
+// l_step) is written out for the standalone merge kernel.
+//
+// CTA organisation (384 threads, one CTA per SM):
+//   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer (Q once, then K/V tiles through a stage ring)
+//   warp  9     MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 at 256 + t*D.
+// P_t (bf16, two per column) overwrites the first 64 columns of S_t; the
+// next S_t is issued after PV_t, and tcgen05 MMAs of one thread run in order.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLn2 = 0.69314718055994530942f;
+// The running max is only moved when a tile's max exceeds it by more than
+// this many powers of two; until then exp2 values stay below 2^8.  O and l
+// share the stale reference, so O / l and m + ln l are unchanged.
+constexpr float kRescaleThreshold = 8.0f;
+
+enum : int {
+  kErrInvalid = 1,
+  kErrTimeout = 6,
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;          // 128-byte swizzle atoms
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kNQ * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[NQ],
+  // p_full[NQ], o_done[NQ], drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kNQ + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 2 * kBN;
+};
+
+// The KV chunks one CTA visits, in ring order.
+struct Ring {
+  int L, c, chunk, i, causal, q_blk_end, num_steps;
+
+  // Ring step s: keys [kv_lo, kv_lo + 128 * n_tiles) of chunk (i - s) mod c
+  // are processed; kv_end is that chunk's end (keys at or beyond it are
+  // masked).
+  __device__ __forceinline__ void seg(int s, int& kv_lo, int& n_tiles,
+                                      int& kv_end) const {
+    n_tiles = 0;
+    kv_lo = 0;
+    kv_end = 0;
+    if (s >= c) return;
+    int j = i - s;
+    if (j < 0) j += c;
+    kv_lo = min(j * chunk, L);
+    kv_end = min((j + 1) * chunk, L);
+    int hi = kv_end;
+    if (causal) {
+      if (j > i) return;
+      if (j == i) hi = min(hi, q_blk_end);
+    }
+    if (hi > kv_lo) n_tiles = (hi - kv_lo + kBN - 1) / kBN;
+  }
+};
+
+// Cursor over the flattened (step, tile) sequence of a Ring.
+struct Cursor {
+  int s, kt, nt, kv_lo, kv_end;
+  __device__ __forceinline__ void skip_empty(const Ring& r) {
+    while (s < r.num_steps) {
+      r.seg(s, kv_lo, nt, kv_end);
+      if (nt > 0) return;
+      ++s;
+    }
+  }
+  __device__ __forceinline__ void start(const Ring& r) {
+    s = 0;
+    kt = 0;
+    skip_empty(r);
+  }
+  __device__ __forceinline__ void advance(const Ring& r) {
+    if (++kt < nt) return;
+    kt = 0;
+    ++s;
+    skip_empty(r);
+  }
+  __device__ __forceinline__ bool first() const { return kt == 0; }
+  __device__ __forceinline__ bool last() const { return kt == nt - 1; }
+};
+
+__device__ __forceinline__ void raise_error(WsHeader* hdr, int code) {
+  atomicCAS(&hdr->error, 0, code);
+}
+
+// Wait that ignores the CTA abort flag (used to drain copies in flight).
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 200000000ull) return false;  // 0.2 s
+  }
+  return true;
+}
+
+}  // namespace
+
+template <int D, bool PARTIALS>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const FwdParams p) {
+  using C = Cfg<D>;
+  const int n_items = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
+  const int item_idx = static_cast<int>(blockIdx.x / p.num_heads);
+  if (item_idx >= n_items) return;
+  // After one CTA gave up on a wait, the rest of the grid does no work.
+  if (*reinterpret_cast<volatile int*>(&p.hdr->error) == kErrTimeout) return;
+  const int h = static_cast<int>(blockIdx.x - item_idx * p.num_heads);
+  const int2 item = p.items[item_idx];
+  const int b = item.x;
+  const int rank = item.y >> 20;
+  const int blk = item.y & 0xFFFFF;
+
+  const int tok0 = p.cu_seqlens[b];
+  Ring ring;
+  ring.L = p.cu_seqlens[b + 1] - tok0;
+  ring.c = p.cp_size ? p.cp_size[b] : 1;
+  ring.chunk = (ring.L + ring.c - 1) / ring.c;
+  ring.i = rank;
+  ring.causal = p.causal;
+  ring.num_steps = p.num_steps;
+  const int qc_hi = min((rank + 1) * ring.chunk, ring.L);
+  const int q0 = min(rank * ring.chunk, ring.L) + blk * kRowsPerItem;
+  ring.q_blk_end = min(q0 + kRowsPerItem, qc_hi);
+  // The second Q tile is skipped when the block has no rows for it.
+  const int nq = (q0 + kBM < ring.q_blk_end) ? kNQ : 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::kStages;
+  uint64_t* v_full = k_empty + C::kStages;
+  uint64_t* v_empty = v_full + C::kStages;
+  uint64_t* s_full = v_empty + C::kStages;
+  uint64_t* p_full = s_full + kNQ;
+  uint64_t* o_done = p_full + kNQ;
+  uint64_t* drain = o_done + kNQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(&k_full[st], 1);
+      mbar_init(&k_empty[st], 1);
+      mbar_init(&v_full[st], 1);
+      mbar_init(&v_empty[st], 1);
+    }
+    for (int t = 0; t < kNQ; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kBM);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint8_t* sq = smem + C::kQOff;
+      uint8_t* sk = smem + C::kKOff;
+      uint8_t* sv = smem + C::kVOff;
+      mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(sq + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
+                      hf * 64, h, tok0 + q0 + t * kBM, pol_q);
+      Cursor cur;
+      cur.start(ring);
+      int nk = 0, nv = 0;  // K and V tiles whose copies were issued
+      bool ok = true;
+      for (; cur.s < ring.num_steps; cur.advance(ring)) {
+        const int x = nk;
+        const int st = x % C::kStages;
+        const uint32_t ph = (x / C::kStages) & 1;
+        const int row = tok0 + cur.kv_lo + cur.kt * kBN;
+        ok = wait_bounded(&k_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(sk + st * C::kTileBytes + hf * 16384, &tm_k, &k_full[st],
+                      hf * 64, h, row, pol_kv);
+        ++nk;
+        ok = wait_bounded(&v_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(sv + st * C::kTileBytes + hf * 16384, &tm_v, &v_full[st],
+                      hf * 64, h, row, pol_kv);
+        ++nv;
+      }
+      if (!ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
+      // Drain: every copy issued into shared memory must land before exit.
+      wait_drain(q_full, 0);
+      for (int st = 0; st < C::kStages; ++st) {
+        if (st < nk) {
+          const int last = st + ((nk - 1 - st) / C::kStages) * C::kStages;
+          wait_drain(&k_full[st], (last / C::kStages) & 1);
+        }
+        if (st < nv) {
+          const int last = st + ((nv - 1 - st) / C::kStages) * C::kStages;
+          wait_drain(&v_full[st], (last / C::kStages) & 1);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, true);
+      const uint32_t sq = smem_u32(smem + C::kQOff);
+      const uint32_t sk = smem_u32(smem + C::kKOff);
+      const uint32_t sv = smem_u32(smem + C::kVOff);
+
+      auto issue_s = [&](int t, int st) {
+        const uint32_t d = tmem + t * kBN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
+          mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, bool acc) {
+        const uint32_t d = tmem + C::kOCol + t * D;
+        const uint32_t a = tmem + t * kBN;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
+          mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      Cursor cur;
+      cur.start(ring);
+      int n = 0;
+      {
+        Cursor c2 = cur;
+        for (; c2.s < ring.num_steps; c2.advance(ring)) ++n;
+      }
+      bool ok = wait_bounded(q_full, 0, abort_flag);
+      if (ok && n > 0) ok = wait_bounded(&k_full[0], 0, abort_flag);
+      if (ok && n > 0) {
+        tc_fence_after();
+        for (int t = 0; t < nq; ++t) issue_s(t, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int x = 0; x < n && ok; ++x, cur.advance(ring)) {
+        const int st = x % C::kStages;
+        const uint32_t ph = (x / C::kStages) & 1;
+        // Fused: one accumulation over every ring step.  Partials: O restarts
+        // at each ring step and is read out at its end.
+        const bool zero_init = PARTIALS ? cur.first() : (x == 0);
+        const bool seg_end = PARTIALS ? cur.last() : (x == n - 1);
+        const bool has_next = x + 1 < n;
+        const int st1 = (x + 1) % C::kStages;
+        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+        ok = wait_bounded(&v_full[st], ph, abort_flag);
+        if (ok && has_next) ok = wait_bounded(&k_full[st1], ph1, abort_flag);
+        for (int t = 0; t < nq && ok; ++t) {
+          ok = wait_bounded(&p_full[t], x & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, st, !zero_init);
+          if (seg_end) mma_commit(&o_done[t]);
+          if (t == nq - 1) mma_commit(&v_empty[st]);
+          if (has_next) {
+            issue_s(t, st1);
+            if (t == nq - 1) mma_commit(&k_empty[st1]);
+          }
+        }
+      }
+      if (!ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else if (warp < 4 * nq) {
+    // ---------------------------------------------------------- softmax --
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + t * kBN;
+    const uint32_t o_addr = tmem + lane_base + C::kOCol + t * D;
+    const int q_pos = q0 + t * kBM + r;
+    const bool row_valid = q_pos < ring.q_blk_end;
+    const size_t row_idx = static_cast<size_t>(tok0 + q_pos) * p.num_heads + h;
+    const float c_log2 = p.scale_log2;
+
+    float m_run = kNegInf;  // running max, log2 domain (scaled score * log2 e)
+    float l_run = 0.f;
+    int x = 0;
+    int seg_done = 0;
+    bool ok = true;
+    bool any_pv = false;  // a PV has accumulated into O_t (this segment)
+
+    for (int s = 0; s < ring.num_steps && ok; ++s) {
+      int kv_lo, nt, kv_end;
+      ring.seg(s, kv_lo, nt, kv_end);
+      if (PARTIALS) {
+        if (nt == 0) {
+          if (row_valid) {
+            const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
+            float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
+            for (int q = 0; q < D / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.m_steps[so] = kNegInf;
+            p.l_steps[so] = 0.f;
+          }
+          continue;
+        }
+        m_run = kNegInf;
+        l_run = 0.f;
+        any_pv = false;
+      }
+      for (int kt = 0; kt < nt; ++kt, ++x) {
+        ok = __all_sync(0xffffffffu, wait_bounded(&s_full[t], x & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[kBN];
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) tmem_ld32(s_addr + q * 32, sr + q * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) reg_fence32(sr + q * 32);
+
+        // Visible keys of this row form a prefix of the tile.
+        const int kv0 = kv_lo + kt * kBN;
+        const int lim = ring.causal ? min(kv_end, q_pos + 1) : kv_end;
+        const int nvis = lim - kv0;
+        if (nvis < kBN) {
+#pragma unroll
+          for (int cc = 0; cc < kBN; ++cc)
+            if (cc >= nvis) sr[cc] = __float_as_uint(kNegInf);
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int cc = 4; cc < kBN; cc += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[cc + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[cc + 3]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = (m_run == kNegInf) ? 0.f : ex2_approx(m_run - m_new);
+          if (any_pv) {
+            // PV of the previous tile completed before S of this tile (same
+            // issuing thread, committed in order), so O_t is stable here.
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t orr[32];
+              tmem_ld32(o_addr + q * 32, orr);
+              tmem_wait_ld();
+              reg_fence32(orr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32(o_addr + q * 32, orr);
+            }
+          }
+          l_run *= alpha;
+          m_run = m_new;
+        }
+        const float mref = (m_run == kNegInf) ? 0.f : m_run;
+        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int k2 = 0; k2 < kBN / 2; ++k2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * k2]), c_log2, -mref));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * k2 + 1]), c_log2, -mref));
+          l0 += p0;
+          l1 += p1;
+          pk[k2] = pack_bf16x2(p0, p1);
+        }
+        l_run += l0 + l1;
+        tmem_st32(s_addr, pk);
+        tmem_st32(s_addr + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+        any_pv = true;
+      }
+      if (PARTIALS && ok) {
+        // End of ring step s: write (O_step, m_step, l_step) and restart.
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(&o_done[t], seg_done & 1, abort_flag));
+        ++seg_done;
+        if (!ok) break;
+        tc_fence_after();
+        const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
+        float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + q * 32, orr);
+          tmem_wait_ld();
+          reg_fence32(orr);
+          if (row_valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              dst[q * 8 + e / 4] =
+                  make_float4(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1]),
+                              __uint_as_float(orr[e + 2]), __uint_as_float(orr[e + 3]));
+          }
+        }
+        if (row_valid) {
+          p.m_steps[so] = (m_run == kNegInf) ? kNegInf : m_run * kLn2;
+          p.l_steps[so] = l_run;
+        }
+        tc_fence_before();
+      }
+    }
+    if (!PARTIALS && ok) {
+      // Epilogue: O / l in bf16 and LSE = m + ln l.
+      ok = __all_sync(0xffffffffu, wait_bounded(&o_done[t], 0, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + row_idx * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + q * 32, orr);
+          tmem_wait_ld();
+          reg_fence32(orr);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                               __uint_as_float(orr[2 * e + 1]) * inv_l);
+          if (row_valid) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+        if (row_valid && p.lse != nullptr)
+          p.lse[row_idx] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+        tc_fence_before();
+      }
+    }
+    if (!ok) {
+      raise_error(p.hdr, kErrTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+int attn_smem_bytes(int D) {
+  return D == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes;
+}
+
+template <int D, bool PARTIALS>
+static cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const FwdParams& p,
+                                 long long grid, cudaStream_t stream) {
+  auto kern = attn_fwd_kernel<D, PARTIALS>;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), Cfg<D>::kSmemBytes,
+         stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const FwdParams& p, int D,
+                        bool partials, long long grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (D == 64)
+    return partials ? launch_attn_t<64, true>(tq, tk, tv, p, grid, stream)
+                    : launch_attn_t<64, false>(tq, tk, tv, p, grid, stream);
+  return partials ? launch_attn_t<128, true>(tq, tk, tv, p, grid, stream)
+                  : launch_attn_t<128, false>(tq, tk, tv, p, grid, stream);
+}
+
+}  // namespace cpattn

@@ -1,0 +1,94 @@
+// Internal interface between the host library (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace cpattn {
+
+// Geometry of the attention kernel.
+constexpr int kBM = 128;               // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;               // keys per KV tile
+constexpr int kNQ = 2;                 // Q tiles per CTA, ping-ponged
+constexpr int kRowsPerItem = kBM * kNQ;
+constexpr int kThreads = 384;          // 2 softmax warpgroups + 1 control WG
+constexpr int kMaxCp = 64;
+
+// Workspace layout (all offsets 256-byte aligned):
+//   [0, 256)                 WsHeader
+//   [256, +4*(B+1))          per-sample prefix of work items
+//   [.., +8*max_items)       work items (int2: sample, (rank << 20) | block)
+//   [.., ...)                unfused mode only: o_steps, m_steps, l_steps
+struct WsHeader {
+  int error;    // cpattn_status of the last kernels run on this workspace
+  int n_items;  // work items built by the schedule kernel
+  int pad[62];
+};
+
+struct WsLayout {
+  size_t prefix_off, items_off, o_off, m_off, l_off, total;
+  int64_t max_items;
+};
+
+WsLayout ws_layout(int64_t T, int32_t B, int32_t H, int32_t D, int32_t max_cp,
+                   bool with_partials);
+
+struct SchedParams {
+  const int* cu_seqlens;
+  const int* cp_size;  // may be null: every sample at CP 1
+  int num_seqs;
+  long long total_tokens;
+  int max_seqlen;
+  int max_cp;
+  int causal;
+  WsHeader* hdr;
+  int* prefix;
+  int2* items;
+  long long max_items;
+};
+
+struct FwdParams {
+  const int* cu_seqlens;
+  const int* cp_size;
+  int num_heads;
+  int num_steps;        // ring steps walked: max_cp (fused) or S (partials)
+  int causal;
+  float scale_log2;     // softmax_scale * log2(e)
+  __nv_bfloat16* out;   // fused: [T, H, D]
+  float* lse;           // fused: [T, H] or null
+  float* o_steps;       // partials: [S, T, H, D]
+  float* m_steps;       // partials: [S, T, H]
+  float* l_steps;
+  long long total_tokens;
+  WsHeader* hdr;
+  const int2* items;
+};
+
+struct MergeParams {
+  const float* o_steps;
+  const float* m_steps;
+  const float* l_steps;
+  int num_steps;
+  long long rows;       // T * H
+  float* out_o;         // public merge: O / l in fp32
+  float* out_m;
+  float* out_l;
+  __nv_bfloat16* out_bf16;  // unfused forward: O / l in bf16
+  float* out_lse;           // unfused forward: m + ln l
+};
+
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
+
+// Dynamic shared memory the attention kernel needs for head_dim D.
+int attn_smem_bytes(int D);
+
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const FwdParams& p, int D,
+                        bool partials, long long grid, cudaStream_t stream);
+
+cudaError_t launch_merge(const MergeParams& p, int D, bool bf16_out,
+                         int num_sms, cudaStream_t stream);
+
+}  // namespace cpattn

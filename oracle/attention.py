@@ -82,30 +82,46 @@ def attention_rows(q, k, v, cu_seqlens, scale, tokens, causal=True):
     """The same definition as :func:`full_attention`, for selected query tokens.
 
     ``tokens`` lists packed token indices; every head of each listed token is
-    computed, one token at a time.  Used to check outputs at sizes where the
-    whole result would take the CPU too long.  Returns
-    ``(out [n, H, D], lse [n, H])`` in the order of ``tokens``.
+    computed.  Used to check outputs at sizes where the whole result would
+    take the CPU too long.  ``q, k, v`` may be any arrays convertible to
+    float64 (for example bf16 torch tensors; they are upcast exactly, one
+    sample at a time).  Returns ``(out [n, H, D], lse [n, H])`` in the order of
+    ``tokens``.
     """
     cu = np.asarray([int(x) for x in cu_seqlens], dtype=np.int64)
     H, D = q.shape[1], q.shape[2]
     tokens = [int(t) for t in tokens]
     out = np.zeros((len(tokens), H, D))
     lse = np.zeros((len(tokens), H))
+    by_sample = {}
     for n, t in enumerate(tokens):
         b = int(np.searchsorted(cu, t, side="right") - 1)
+        by_sample.setdefault(b, []).append(n)
+    for b, idx in by_sample.items():
         s0, s1 = int(cu[b]), int(cu[b + 1])
-        p = t - s0
-        kend = s0 + p + 1 if causal else s1
-        qt = np.asarray(q[t], dtype=np.float64)            # [H, D]
-        kk = np.asarray(k[s0:kend], dtype=np.float64)      # [n_k, H, D]
-        vv = np.asarray(v[s0:kend], dtype=np.float64)
-        s = scale * np.einsum("hd,jhd->hj", qt, kk)        # [H, n_k]
-        mx = s.max(axis=1, keepdims=True)
-        row_lse = mx + np.log(np.exp(s - mx).sum(axis=1, keepdims=True))
-        p_ = np.exp(s - row_lse)
-        out[n] = np.einsum("hj,jhd->hd", p_, vv)
-        lse[n] = row_lse[:, 0]
+        kend_max = max(tokens[n] for n in idx) + 1 if causal else s1
+        # [H, n_k, D] float64 copies of this sample's visible keys and values.
+        kt = np.ascontiguousarray(np.transpose(_f64(k[s0:kend_max]), (1, 0, 2)))
+        vt = np.ascontiguousarray(np.transpose(_f64(v[s0:kend_max]), (1, 0, 2)))
+        for n in idx:
+            t = tokens[n]
+            nk = (t - s0 + 1) if causal else (s1 - s0)
+            qt = _f64(q[t])                                          # [H, D]
+            s = scale * np.matmul(kt[:, :nk], qt[:, :, None])[:, :, 0]  # [H, nk]
+            mx = s.max(axis=1, keepdims=True)
+            row_lse = mx + np.log(np.exp(s - mx).sum(axis=1, keepdims=True))
+            p_ = np.exp(s - row_lse)
+            out[n] = np.matmul(p_[:, None, :], vt[:, :nk])[:, 0, :]
+            lse[n] = row_lse[:, 0]
     return out, lse
+
+
+def _f64(x):
+    """Exact float64 copy of a NumPy array or a (CPU) torch tensor."""
+    if hasattr(x, "detach"):
+        import torch  # only when handed torch tensors
+        return x.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------

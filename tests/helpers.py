@@ -1,0 +1,57 @@
+"""Shared helpers for the GPU parity tests (tolerances, batch construction)."""
+
+import math
+
+import numpy as np
+import torch
+
+from long_context_gb300 import workloads
+
+# Tolerances for bf16 inputs with fp32 accumulation, against the float64 oracle.
+O_ATOL = 2e-2          # attention output, max abs
+LSE_RTOL = 1e-3        # |dLSE| <= 1e-3 * max(1, |LSE|)
+MERGE_ATOL = 1e-5      # fp32 merge output O / l, max abs
+MERGE_L_RTOL = 1e-5    # fp32 merge output l, relative
+
+
+def check_attention(out, lse, ref_o, ref_lse, what=""):
+    """Assert the attention tolerances; returns (max |dO|, max scaled |dLSE|)."""
+    out = np.asarray(out, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    assert np.all(np.isfinite(out)), "%s: non-finite output" % what
+    do = float(np.max(np.abs(out - ref_o))) if out.size else 0.0
+    dl = float(np.max(np.abs(lse - ref_lse) / np.maximum(1.0, np.abs(ref_lse)))) if lse.size else 0.0
+    assert do <= O_ATOL, "%s: max |dO| = %g" % (what, do)
+    assert dl <= LSE_RTOL, "%s: max rel |dLSE| = %g" % (what, dl)
+    return do, dl
+
+
+def make_batch(lengths, H, D, seed, std=1.0, device="cuda"):
+    """Seeded THD batch: CPU bf16 q/k/v, int32 cu_seqlens, and GPU copies."""
+    T = int(sum(lengths))
+    q, k, v = workloads.qkv(T, H, D, seed, std)
+    cu = workloads.cu_seqlens(lengths)
+    g = dict(q=q.to(device), k=k.to(device), v=v.to(device),
+             cu=torch.from_numpy(cu).to(device))
+    return (q, k, v, cu), g
+
+
+def sample_tokens(cu, n_random, seed, extra=()):
+    """Token indices to check at full size: the first, second, last and last-but-
+    one token of every sample, tile and chunk edges near them, plus random ones."""
+    rng = np.random.default_rng(seed)
+    cu = [int(x) for x in cu]
+    T = cu[-1]
+    toks = set(int(t) for t in extra if 0 <= t < T)
+    for b in range(len(cu) - 1):
+        s0, s1 = cu[b], cu[b + 1]
+        for t in (s0, s0 + 1, s0 + 127, s0 + 128, s1 - 2, s1 - 1):
+            if s0 <= t < s1:
+                toks.add(t)
+    if T > 0:
+        toks.update(int(t) for t in rng.integers(0, T, n_random))
+    return sorted(toks)
+
+
+def default_scale(D):
+    return 1.0 / math.sqrt(D)
