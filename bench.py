@@ -1,0 +1,496 @@
+#!/usr/bin/env python3
+"""Throughput of the CP ring-attention hot path on GB300 GPUs.
+
+One step = one pass of the hot path over one packed THD micro-batch: the
+dynamic-CP plan (``cpattn_plan``, host) and the ring-attention forward with the
+online-softmax merge fused (``cpattn_fwd``), on the 16,384-token packed batch
+(lognormal lengths, world 4, per-rank limit 4096, CP sizes from {1, 2, 4},
+H=32, D=128, causal).  ``value`` is attention TFLOP/s (4 * H * D per visible
+query/key pair) over all GPUs; every GPU runs its own independent batch
+(seed + rank), so scaling is weak and there is no collective on the data path.
+
+The same JSON line also reports: ``e2e`` (host buffers, copies in the timed
+region), the attention kernel's roofline, the float64 CPU oracle timed on a
+bounded sample (``cpu_baseline``), GPU clocks during the timed regions, and
+sub-measurements of the 131,072-token CP=4 sequence, the unfused path and the
+CP=8 merge of stored partials.
+
+``--impl reference`` times the oracle itself on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("causal ring-attn fwd TFLOP/s (% bf16 peak) on THD batches; "
+          "merge GB/s (% HBM)")
+WORKLOAD = "packed16k"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the 128K, unfused and merge sub-measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, choices=[None, "main", "long128k", "merge8"],
+                    help="run one measurement only (for profiling)")
+    return ap.parse_args()
+
+
+def attention_flops(lengths, H, D, causal=True):
+    pairs = sum((L * (L + 1) // 2) if causal else L * L for L in lengths)
+    return 4.0 * H * D * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def profiled_traffic(name, source_file):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since it was taken (the summary records the source hash)."""
+    prof = os.path.join(ROOT, "profiles", name)
+    src = os.path.join(ROOT, "long_context_gb300", "csrc", source_file)
+    try:
+        text = open(prof).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != digest:
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while timed work runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+        self.windows = []
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, begin):
+        now = time.time()
+        if begin:
+            self.t0 = now
+        else:
+            self.windows.append((self.t0, now))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names[1:], r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)]
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_setup(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------ reference --
+
+def cpu_oracle_sample(lengths, H, D, seed, budget_s):
+    """Time the float64 oracle's full attention on the batch's shortest samples
+    until about ``budget_s`` seconds of work; returns (TFLOP/s, desc, cores)."""
+    import numpy as np
+    from long_context_gb300 import workloads
+    from oracle import attention as oa
+    order = sorted(range(len(lengths)), key=lambda b: lengths[b])
+    flops = 0.0
+    used = []
+    t_total = 0.0
+    scale = 1.0 / np.sqrt(D)
+    for b in order:
+        L = lengths[b]
+        q, k, v = workloads.qkv(L, H, D, seed + 7919 * b)
+        qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+        cu = np.array([0, L], dtype=np.int64)
+        t0 = time.perf_counter()
+        oa.full_attention(qf, kf, vf, cu, scale)
+        t_total += time.perf_counter() - t0
+        flops += attention_flops([L], H, D)
+        used.append(L)
+        if t_total >= budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = ("float64 oracle full attention (NumPy/BLAS) on %d of the batch's samples, "
+            "lengths %s, H=%d, D=%d; %.1f s" % (len(used), used, H, D, t_total))
+    return flops / t_total / 1e12, desc, cores, t_total
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from long_context_gb300 import workloads
+    w = workloads.WORKLOADS[WORKLOAD]
+    lengths = workloads.packed_lengths(args.seed, w["budget"])
+    H, D = w["H"], w["D"]
+    import numpy as np
+    from oracle import attention as oa
+    # One step = the oracle's full attention on the batch's shortest sample.
+    L = min(lengths)
+    q, k, v = workloads.qkv(L, H, D, args.seed)
+    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+    cu = np.array([0, L], dtype=np.int64)
+    scale = 1.0 / np.sqrt(D)
+    for _ in range(args.warmup):
+        oa.full_attention(qf, kf, vf, cu, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oa.full_attention(qf, kf, vf, cu, scale)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = attention_flops([L], H, D) / dt / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = ("float64 oracle full attention on the batch's shortest sample (L=%d of %s), "
+              "H=%d, D=%d, causal" % (L, lengths, H, D))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "packed16k sample (CPU oracle)", "sample_len": L, "H": H, "D": D},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- measured --
+
+def time_loop(torch, fn, steps, warmup, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / max(steps, 1)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from long_context_gb300 import build as lib_build
+    lib_build.build()
+    from long_context_gb300 import cpattn, workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    hbm_peak, bf16_peak, bf16_sustained, peak_src = load_peaks()
+
+    w = workloads.WORKLOADS[WORKLOAD]
+    H, D, W, limit, max_cp = w["H"], w["D"], w["world"], w["limit"], w["max_cp"]
+    seed = args.seed + rank
+    lengths = workloads.packed_lengths(seed, w["budget"])
+    T = sum(lengths)
+    B = len(lengths)
+    scale = 1.0 / np.sqrt(D)
+    q, k, v = workloads.qkv_device(T, H, D, seed, device=dev)
+    cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+    cp_pinned = torch.zeros(B, dtype=torch.int32).pin_memory()
+    cp_dev = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = cpattn.alloc_workspace(T, B, H, D, max_cp, cpattn.MODE_FUSED, device=dev)
+    flops = attention_flops(lengths, H, D)
+
+    def step():
+        plan = cpattn.plan(lengths, W, limit, max_cp)           # dynamic-CP plan (host)
+        cp_pinned.numpy()[:] = plan["cp_size"]
+        cp_dev.copy_(cp_pinned, non_blocking=True)
+        cpattn.fwd(q, k, v, cu, cp_dev, max_seqlen=max(lengths), max_cp=max_cp,
+                   softmax_scale=scale, out=out, lse=lse, workspace=ws)
+
+    def kernel_only():
+        cpattn.fwd(q, k, v, cu, cp_dev, max_seqlen=max(lengths), max_cp=max_cp,
+                   softmax_scale=scale, out=out, lse=lse, workspace=ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if args.only in ("long128k", "merge8"):
+        fn = run_long128k if args.only == "long128k" else run_merge8
+        res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                 bf16_sustained, hbm_peak)
+        clk = clocks.stop()
+        if rank == 0:
+            print(json.dumps({"only": args.only, **res, "clocks": clk}), flush=True)
+        return 0
+
+    # --- main timed region: exactly K steps, barrier + sync on both sides.
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
+    if world > 1:
+        dist.barrier()
+    status = cpattn.poll_error(ws)
+    if status != cpattn.OK:
+        raise RuntimeError("device status after timed steps: %s" % cpattn.status_string(status))
+    ms_max = ms
+    total_flops = flops
+    if world > 1:
+        t = torch.tensor([ms, flops], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        ms_max = float(mx[0])
+        total_flops = float(t[1])
+    value = total_flops * args.steps / (ms_max * args.steps * 1e-3) / 1e12
+
+    # --- the attention kernel alone (roofline): average launch duration.
+    k_ms = time_loop(torch, kernel_only, args.steps, 3, stream)
+    achieved = flops / (k_ms * 1e-3) / 1e12
+    traffic = profiled_traffic("attn_fwd_packed16k.md", "attn_fwd.cu")
+
+    if args.only == "main":
+        clk = clocks.stop()
+        if rank == 0:
+            print(json.dumps({"only": "main", "value": value, "ms_per_step": ms_max,
+                              "kernel_ms": k_ms, "achieved": achieved, "clocks": clk}),
+                  flush=True)
+        return 0
+
+    # --- end to end through the public API with host buffers.
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    hcu = cu.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+    dcu = torch.empty_like(cu)
+
+    def e2e_step():
+        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dcu, hcu)):
+            d_.copy_(h_, non_blocking=True)
+        plan = cpattn.plan(lengths, W, limit, max_cp)
+        cp_pinned.numpy()[:] = plan["cp_size"]
+        cp_dev.copy_(cp_pinned, non_blocking=True)
+        cpattn.fwd(dq, dk, dv, dcu, cp_dev, max_seqlen=max(lengths), max_cp=max_cp,
+                   softmax_scale=scale, out=out, lse=lse, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    clocks.mark(True)
+    e2e_ms = time_loop(torch, e2e_step, args.steps, 3, stream)
+    clocks.mark(False)
+    h2d = 3 * T * H * D * 2 + (B + 1) * 4 + B * 4
+    d2h = T * H * D * 2 + T * H * 4
+    e2e_ms_max = e2e_ms
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms_max = float(t[0])
+    e2e_value = total_flops / (e2e_ms_max * 1e-3) / 1e12
+    del hq, hk, hv, dq, dk, dv
+
+    extras = {}
+    if not args.no_extras:
+        for fn in (run_long128k, run_merge8):
+            extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
+                             bf16_peak, bf16_sustained, hbm_peak))
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tflops, desc, cores, _ = cpu_oracle_sample(lengths, H, D, seed, budget_s=12.0)
+        cpu = {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+    plan = cpattn.plan(lengths, W, limit, max_cp)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "packed THD micro-batch, 16384-token budget, lognormal(7.5,1) lengths "
+                        "clipped to [64,16384], DPxCP world 4, max_seqlen_per_dp_cp_rank 4096, "
+                        "CP from {1,2,4}, H=32, D=128, causal, bf16 N(0,1)",
+            "lengths": lengths, "cp_sizes": [int(x) for x in plan["cp_size"]],
+            "tokens_per_gpu": T, "H": H, "D": D, "seed": args.seed,
+            "parallelism": "one independent micro-batch per GPU (seed + rank), no collective",
+            "l2": "inputs larger than L2 (Q/K/V %.0f MB per GPU)" % (3 * T * H * D * 2 / 1e6),
+            "step": "cpattn_plan (host) + cp_size upload + cpattn_fwd fused",
+        },
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,false> + schedule_kernel",
+                     "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_peak, "traffic": traffic,
+                     "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                     "kernel_ms": k_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    line.update(extras)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                 bf16_sustained, hbm_peak):
+    import numpy as np
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    # 131,072-token causal sequence at CP=4, fused and unfused.
+    w = workloads.WORKLOADS["long128k"]
+    H, D, L, c = w["H"], w["D"], w["lengths"][0], w["cp"]
+    q, k, v = workloads.qkv_device(L, H, D, args.seed, std=w["std"], device=dev)
+    cu = torch.tensor([0, L], dtype=torch.int32, device=dev)
+    cps = torch.tensor([c], dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((L, H), dtype=torch.float32, device=dev)
+    flops = attention_flops([L], H, D)
+    sub = {}
+    for mode, name in ((cpattn.MODE_FUSED, "fused"), (cpattn.MODE_UNFUSED, "unfused")):
+        ws = cpattn.alloc_workspace(L, 1, H, D, c, mode, device=dev)
+        fn = lambda: cpattn.fwd(q, k, v, cu, cps, max_seqlen=L, max_cp=c,  # noqa: E731
+                                softmax_scale=1.0 / np.sqrt(D), mode=mode, out=out, lse=lse,
+                                workspace=ws)
+        clocks.mark(True)
+        ms = time_loop(torch, fn, steps, 2, stream)
+        clocks.mark(False)
+        assert cpattn.poll_error(ws) == cpattn.OK
+        tf = flops / (ms * 1e-3) / 1e12
+        sub[name] = {"ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+                     "frac_of_sustained": tf / bf16_sustained}
+        del ws
+    res["long128k"] = {"workload": "one causal 131072-token sequence, CP=4 (32768-token chunks), "
+                                   "H=16, D=128, bf16 N(0,0.5^2)",
+                       "flops": flops, "steps": steps, **sub}
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+               bf16_sustained, hbm_peak):
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    # Merge of CP=8 stored partials, T=32768, H=32, D=128.
+    w = workloads.WORKLOADS["merge8"]
+    S, T, H, D = w["S"], w["T"], w["H"], w["D"]
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    o = torch.randn((S, T, H, D), generator=g, device=dev, dtype=torch.float32)
+    m = torch.rand((S, T, H), generator=g, device=dev, dtype=torch.float32) * 10 - 5
+    l = torch.rand((S, T, H), generator=g, device=dev, dtype=torch.float32) * 1023 + 1
+    oo = torch.empty((T, H, D), device=dev, dtype=torch.float32)
+    om = torch.empty((T, H), device=dev, dtype=torch.float32)
+    ol = torch.empty((T, H), device=dev, dtype=torch.float32)
+    nbytes = S * T * H * (D + 2) * 4 + T * H * (D + 2) * 4
+    fn = lambda: cpattn.merge(o, m, l, out_o=oo, out_m=om, out_l=ol)  # noqa: E731
+    clocks.mark(True)
+    ms = time_loop(torch, fn, max(steps, 10), 3, stream)
+    clocks.mark(False)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["merge8"] = {"workload": "CP=8 partials, T=32768, H=32, D=128 fp32 (inputs 4.4 GB > L2)",
+                     "bytes": nbytes, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
+                     "traffic": profiled_traffic("merge_merge8.md", "merge.cu")}
+    del o, m, l, oo, om, ol
+    torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    sys.exit(main())

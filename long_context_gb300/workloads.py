@@ -9,7 +9,9 @@ Recipe (shared by tests and the benchmark):
 * sample lengths come from ``numpy.random.default_rng(seed)``;
 * Q, K and V come from a CPU ``torch.Generator().manual_seed(seed)``, drawn in
   that order as float32 standard normals, multiplied by ``std`` and rounded to
-  bfloat16 (round to nearest even);
+  bfloat16 (round to nearest even); for the largest inputs the same recipe
+  runs on a seeded CUDA generator (``qkv_device``) and the rows the oracle
+  needs are copied back, so both sides still see the same bytes;
 * merge partials come from a CPU ``torch.Generator().manual_seed(seed)``:
   O_step ~ N(0, 1), then m_step ~ U[-5, 5], then l_step ~ U[1, 1024], float32.
 
@@ -82,6 +84,20 @@ def qkv(total_tokens, num_heads, head_dim, seed, std=1.0):
     out = []
     for _ in range(3):
         x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        out.append(x.to(torch.bfloat16))
+    return tuple(out)
+
+
+def qkv_device(total_tokens, num_heads, head_dim, seed, std=1.0, device="cuda"):
+    """Q, K, V drawn on the GPU from a seeded CUDA generator (same recipe as
+    :func:`qkv`, different stream of numbers); bfloat16 ``[T, H, D]``."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    shape = (int(total_tokens), int(num_heads), int(head_dim))
+    out = []
+    for _ in range(3):
+        x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
         if std != 1.0:
             x.mul_(std)
         out.append(x.to(torch.bfloat16))

@@ -103,11 +103,13 @@ def test_zero_tokens(cp):
 
 
 def test_large_scores_and_rescale(cp):
-    """Scores spread over many powers of two exercise the running-max update."""
+    """Scores spread over many powers of two exercise the running-max update.
+    The spread comes from the softmax scale (as if Q and K had std 2.5); V
+    stays N(0, 1), the distribution the output tolerance is stated for."""
     lengths = [700, 1500]
     H, D = 2, 128
-    (q, k, v, cu), g = make_batch(lengths, H, D, seed=5, std=2.5)
-    scale = default_scale(D)
+    (q, k, v, cu), g = make_batch(lengths, H, D, seed=5)
+    scale = 6.25 * default_scale(D)
     out, lse = _run(cp, g, lengths, [2, 4], H, D, True, 0, scale)
     qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
     ref_o, ref_lse = oa.full_attention(qf, kf, vf, cu, scale)
@@ -257,10 +259,13 @@ def test_sweep256_workload(cp):
         members = [b for b in range(len(lengths)) if plan_c["micro_batch"][b] == mb]
         lens = [lengths[b] for b in members]
         cps = [int(plan_c["cp_size"][b]) for b in members]
-        # Each micro-batch draws its own seeded tensors (seed = micro-batch id).
-        (q, k, v, cu), g = make_batch(lens, H, D, seed=1000 + mb)
+        # Each micro-batch draws its own tensors on the GPU (seed = 1000 + id);
+        # the oracle reads back only the samples it checks.
+        q, k, v = workloads.qkv_device(sum(lens), H, D, seed=1000 + mb)
+        cu = workloads.cu_seqlens(lens)
+        cu_t = torch.from_numpy(cu).cuda()
         cps_t = torch.tensor(cps, dtype=torch.int32, device="cuda")
-        out, lse = cp.fwd(g["q"], g["k"], g["v"], g["cu"], cps_t, max_seqlen=max(lens),
+        out, lse = cp.fwd(q, k, v, cu_t, cps_t, max_seqlen=max(lens),
                           max_cp=w["max_cp"], softmax_scale=scale)
         if mb % 8 == 0 or mb == plan_c["num_micro_batches"] - 1:
             toks = sorted(set(int(t) for t in rng.integers(0, int(cu[-1]), 6)) |
