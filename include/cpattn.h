@@ -212,6 +212,42 @@ int cpattn_merge(const float* o_steps, const float* m_steps,
                  float* out_m, float* out_l, void* stream);
 
 /*
+ * cpattn_fwd_noalloc -- cpattn_fwd (CPATTN_MODE_FUSED) for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot hand the library a workspace: code running inside a host program
+ * whose memory pool owns the whole device budget and forbids further
+ * allocations, or latency-critical code that must avoid cudaMalloc/cudaFree
+ * because they can synchronise the device.  It computes exactly what
+ * cpattn_fwd computes in the fused mode, but keeps its scratch (error word
+ * and work list) in a fixed 1 MiB array inside the library's device image,
+ * which every GPU that loads the library holds until the process exits.  It
+ * allocates nothing.
+ *
+ * Arguments as cpattn_fwd, without mode / workspace / workspace_bytes, plus:
+ *   status  device int32 [1] or NULL: receives the call's device status (the
+ *           error word cpattn_poll_error would report) once the kernels have
+ *           finished, in stream order.
+ * Limits and behaviour:
+ *   - Problems whose fused workspace (cpattn_fwd_workspace_size(T, B, H, D,
+ *     max_cp, CPATTN_MODE_FUSED)) exceeds 1 MiB are rejected with
+ *     CPATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call clears the parts that must start at zero itself.  Calls whose
+ *     kernels overlap on the GPU (for example on two streams at once) race on
+ *     the array: serialise them.
+ */
+int cpattn_fwd_noalloc(const void* q, const void* k, const void* v,
+                       const int32_t* cu_seqlens, const int32_t* cp_size,
+                       int32_t num_seqs, int64_t total_tokens, int32_t max_seqlen,
+                       int32_t max_cp, int32_t num_heads, int32_t head_dim,
+                       float softmax_scale, int32_t causal, void* out, float* lse,
+                       int32_t* status, void* stream);
+
+/*
  * cpattn_poll_error -- synchronise `stream` and return the workspace's error
  * word (CPATTN_OK when every kernel since the last cpattn_fwd on this
  * workspace finished normally), or CPATTN_ERR_CUDA if the stream reports a

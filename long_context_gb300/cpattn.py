@@ -51,6 +51,9 @@ _lib.cpattn_fwd_partials.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, 
                                      _i32, _i32, ctypes.c_float, _i32, _i32, _vp, _vp,
                                      _vp, _vp, ctypes.c_size_t, _vp]
 _lib.cpattn_fwd_partials.restype = ctypes.c_int
+_lib.cpattn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, _i32,
+                                    _i32, ctypes.c_float, _i32, _vp, _vp, _vp, _vp]
+_lib.cpattn_fwd_noalloc.restype = ctypes.c_int
 _lib.cpattn_merge.argtypes = [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
 _lib.cpattn_merge.restype = ctypes.c_int
 _lib.cpattn_poll_error.argtypes = [_vp, _vp]
@@ -201,6 +204,33 @@ def fwd(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None, softmax_s
                          1 if causal else 0, int(mode), _ptr(out), _ptr(lse),
                          _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "cpattn_fwd")
+    return out, lse
+
+
+def fwd_noalloc(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
+                softmax_scale=None, causal=True, out, lse=None, status=None, stream=None):
+    """``cpattn_fwd_noalloc``: the fused forward with the library's fixed
+    scratch instead of a workspace, for callers that cannot allocate device
+    memory.  ``out`` (and ``lse``, ``status`` if given) are caller-provided;
+    ``status`` is a device int32 tensor of one element receiving the device
+    status.  Returns ``(out, lse)``."""
+    dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    if max_cp is None:
+        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    _need(out, "out", torch.bfloat16, dev, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev, (T, H))
+    if status is not None:
+        _need(status, "status", torch.int32, dev, (1,))
+    st = _lib.cpattn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cp_size),
+                                 B, T, int(max_seqlen), int(max_cp), H, D,
+                                 float(softmax_scale), 1 if causal else 0, _ptr(out),
+                                 _ptr(lse), _ptr(status), _stream(stream))
+    _check(st, "cpattn_fwd_noalloc")
     return out, lse
 
 

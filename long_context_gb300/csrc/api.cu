@@ -20,10 +20,6 @@ constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-inline bool aligned(const void* p, size_t a) {
-  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
-}
-
 struct DeviceInfo {
   int num_sms = 0;
   int cc_major = 0;
@@ -78,15 +74,11 @@ int make_qkv_map(CUtensorMap* map, const void* base, int64_t T, int H, int D) {
   return r == CUDA_SUCCESS ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-struct FwdArgs {
-  const void *q, *k, *v;
-  const int32_t *cu, *cp;
-  int32_t B;
-  int64_t T;
-  int32_t max_seqlen, max_cp, H, D;
-  float scale;
-  int32_t causal;
-};
+}  // namespace
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
 
 int check_fwd(const FwdArgs& a) {
   if (a.B < 0 || a.T < 0 || a.H < 1 || a.max_cp < 1 || a.max_cp > kMaxCp)
@@ -160,8 +152,6 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;
 }
-
-}  // namespace
 
 WsLayout ws_layout(int64_t T, int32_t B, int32_t H, int32_t D, int32_t max_cp,
                    bool with_partials) {

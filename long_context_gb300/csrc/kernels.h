@@ -79,6 +79,31 @@ struct MergeParams {
   float* out_lse;           // unfused forward: m + ln l
 };
 
+// Host-side forward arguments and the launch sequence shared by the entry
+// points (api.cu).
+struct FwdArgs {
+  const void *q, *k, *v;
+  const int32_t *cu, *cp;
+  int32_t B;
+  int64_t T;
+  int32_t max_seqlen, max_cp, H, D;
+  float scale;
+  int32_t causal;
+};
+
+bool aligned(const void* p, size_t a);
+
+// Host-checkable argument rules of the forward calls; a cpattn_status.
+int check_fwd(const FwdArgs& a);
+
+// Schedule kernel + attention kernel on `stream`, using `workspace` (at least
+// ws_layout(T, B, H, D, max_cp, false).total bytes) for the error word and the
+// work list; a cpattn_status.
+int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
+                  __nv_bfloat16* out, float* lse, float* o_steps,
+                  float* m_steps, float* l_steps, void* workspace,
+                  cudaStream_t stream);
+
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 
 // Dynamic shared memory the attention kernel needs for head_dim D.
