@@ -111,18 +111,20 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
 
+  const long long grid = lay.max_items * a.H;
+  if (grid > 0x7fffffffLL) return CPATTN_ERR_UNSUPPORTED;
   SchedParams sp;
   sp.cu_seqlens = a.cu;
   sp.cp_size = a.cp;
   sp.num_seqs = a.B;
+  sp.num_heads = a.H;
   sp.total_tokens = a.T;
   sp.max_seqlen = a.max_seqlen;
   sp.max_cp = a.max_cp;
-  sp.causal = a.causal;
   sp.hdr = hdr;
-  sp.prefix = reinterpret_cast<int*>(ws + lay.prefix_off);
-  sp.items = reinterpret_cast<int2*>(ws + lay.items_off);
-  sp.max_items = lay.max_items;
+  sp.first_cta = reinterpret_cast<int*>(ws + lay.prefix_off);
+  sp.order = reinterpret_cast<int*>(ws + lay.items_off);
+  sp.max_ctas = grid;
   if (launch_schedule(sp, stream) != cudaSuccess) return CPATTN_ERR_CUDA;
   if (a.T == 0 || a.B == 0) return CPATTN_OK;
 
@@ -146,8 +148,9 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   fp.l_steps = l_steps;
   fp.total_tokens = a.T;
   fp.hdr = hdr;
-  fp.items = sp.items;
-  const long long grid = lay.max_items * a.H;
+  fp.first_cta = sp.first_cta;
+  fp.order = sp.order;
+  fp.num_seqs = a.B;
   if (launch_attn(tq, tk, tv, fp, a.D, partials, grid, stream) != cudaSuccess)
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;

@@ -21,6 +21,8 @@
 //   warp  8     TMA producer (Q once, then K/V tiles through a stage ring)
 //   warp  9     MMA issuer (one thread) and TMEM owner
 //   warps 10-11 idle
+// The softmax warpgroups take 224 registers per thread and the control
+// warpgroup (warps 8-11) gives its share up, down to 56.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 at 256 + t*D.
 // P_t (bf16, two per column) overwrites the first 64 columns of S_t; the
 // next S_t is issued after PV_t, and tcgen05 MMAs of one thread run in order.
@@ -28,6 +30,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "work.cuh"
 
 namespace cpattn {
 
@@ -136,22 +139,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const FwdParams p) {
   using C = Cfg<D>;
-  const int n_items = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
-  const int item_idx = static_cast<int>(blockIdx.x / p.num_heads);
-  if (item_idx >= n_items) return;
+  const int n_ctas = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
+  const int x_cta = static_cast<int>(blockIdx.x);
+  if (x_cta >= n_ctas) return;
   // After one CTA gave up on a wait, the rest of the grid does no work.
   if (*reinterpret_cast<volatile int*>(&p.hdr->error) == kErrTimeout) return;
-  const int h = static_cast<int>(blockIdx.x - item_idx * p.num_heads);
-  const int2 item = p.items[item_idx];
-  const int b = item.x;
-  const int rank = item.y >> 20;
-  const int blk = item.y & 0xFFFFF;
+
+  // CTA -> (sample, head, rank, block): see work.cuh for the order.
+  int pos = 0;
+  {
+    int hi = p.num_seqs - 1;
+    while (pos < hi) {
+      const int mid = (pos + hi + 1) >> 1;
+      if (p.first_cta[mid] <= x_cta) pos = mid; else hi = mid - 1;
+    }
+  }
+  const int b = p.order[pos];
+  const SampleGeom geo = sample_geom(p.cu_seqlens, p.cp_size, b);
+  const int n_b = sample_items(geo);
+  const int e_cta = x_cta - p.first_cta[pos];
+  const int h = e_cta / n_b;
+  int rank, blk;
+  item_coords(geo, n_b - 1 - (e_cta - h * n_b), rank, blk);
 
   const int tok0 = p.cu_seqlens[b];
   Ring ring;
-  ring.L = p.cu_seqlens[b + 1] - tok0;
-  ring.c = p.cp_size ? p.cp_size[b] : 1;
-  ring.chunk = (ring.L + ring.c - 1) / ring.c;
+  ring.L = geo.L;
+  ring.c = geo.c;
+  ring.chunk = geo.chunk;
   ring.i = rank;
   ring.causal = p.causal;
   ring.num_steps = p.num_steps;
@@ -205,311 +220,324 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  static_assert(kSoftmaxRegs == 224 && kCtrlRegs == 56, "immediates below");
 
-  if (warp == 8) {
-    // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint64_t pol_q = l2_policy_evict_first();
-      const uint64_t pol_kv = l2_policy_evict_last();
-      uint8_t* sq = smem + C::kQOff;
-      uint8_t* sk = smem + C::kKOff;
-      uint8_t* sv = smem + C::kVOff;
-      mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
-      for (int t = 0; t < nq; ++t)
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sq + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
-                      hf * 64, h, tok0 + q0 + t * kBM, pol_q);
-      Cursor cur;
-      cur.start(ring);
-      int nk = 0, nv = 0;  // K and V tiles whose copies were issued
-      bool ok = true;
-      for (; cur.s < ring.num_steps; cur.advance(ring)) {
-        const int x = nk;
-        const int st = x % C::kStages;
-        const uint32_t ph = (x / C::kStages) & 1;
-        const int row = tok0 + cur.kv_lo + cur.kt * kBN;
-        ok = wait_bounded(&k_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sk + st * C::kTileBytes + hf * 16384, &tm_k, &k_full[st],
-                      hf * 64, h, row, pol_kv);
-        ++nk;
-        ok = wait_bounded(&v_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sv + st * C::kTileBytes + hf * 16384, &tm_v, &v_full[st],
-                      hf * 64, h, row, pol_kv);
-        ++nv;
-      }
-      if (!ok) {
-        raise_error(p.hdr, kErrTimeout);
-        *abort_flag = 1;
-      }
-      // Drain: every copy issued into shared memory must land before exit.
-      wait_drain(q_full, 0);
-      for (int st = 0; st < C::kStages; ++st) {
-        if (st < nk) {
-          const int last = st + ((nk - 1 - st) / C::kStages) * C::kStages;
-          wait_drain(&k_full[st], (last / C::kStages) & 1);
-        }
-        if (st < nv) {
-          const int last = st + ((nv - 1 - st) / C::kStages) * C::kStages;
-          wait_drain(&v_full[st], (last / C::kStages) & 1);
-        }
-      }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, true);
-      const uint32_t sq = smem_u32(smem + C::kQOff);
-      const uint32_t sk = smem_u32(smem + C::kKOff);
-      const uint32_t sv = smem_u32(smem + C::kVOff);
-
-      auto issue_s = [&](int t, int st) {
-        const uint32_t d = tmem + t * kBN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
-          mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[t]);
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t d = tmem + C::kOCol + t * D;
-        const uint32_t a = tmem + t * kBN;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
-          mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-
-      Cursor cur;
-      cur.start(ring);
-      int n = 0;
-      {
-        Cursor c2 = cur;
-        for (; c2.s < ring.num_steps; c2.advance(ring)) ++n;
-      }
-      bool ok = wait_bounded(q_full, 0, abort_flag);
-      if (ok && n > 0) ok = wait_bounded(&k_full[0], 0, abort_flag);
-      if (ok && n > 0) {
-        tc_fence_after();
-        for (int t = 0; t < nq; ++t) issue_s(t, 0);
-        mma_commit(&k_empty[0]);
-      }
-      for (int x = 0; x < n && ok; ++x, cur.advance(ring)) {
-        const int st = x % C::kStages;
-        const uint32_t ph = (x / C::kStages) & 1;
-        // Fused: one accumulation over every ring step.  Partials: O restarts
-        // at each ring step and is read out at its end.
-        const bool zero_init = PARTIALS ? cur.first() : (x == 0);
-        const bool seg_end = PARTIALS ? cur.last() : (x == n - 1);
-        const bool has_next = x + 1 < n;
-        const int st1 = (x + 1) % C::kStages;
-        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-        ok = wait_bounded(&v_full[st], ph, abort_flag);
-        if (ok && has_next) ok = wait_bounded(&k_full[st1], ph1, abort_flag);
-        for (int t = 0; t < nq && ok; ++t) {
-          ok = wait_bounded(&p_full[t], x & 1, abort_flag);
+  if (warp >= 8) {
+    regs_lower_56();
+    if (warp == 8) {
+      // ------------------------------------------------------ TMA producer --
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        uint8_t* sq = smem + C::kQOff;
+        uint8_t* sk = smem + C::kKOff;
+        uint8_t* sv = smem + C::kVOff;
+        mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
+        for (int t = 0; t < nq; ++t)
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(sq + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
+                        hf * 64, h, tok0 + q0 + t * kBM, pol_q);
+        Cursor cur;
+        cur.start(ring);
+        int nk = 0, nv = 0;  // K and V tiles whose copies were issued
+        bool ok = true;
+        for (; cur.s < ring.num_steps; cur.advance(ring)) {
+          const int x = nk;
+          const int st = x % C::kStages;
+          const uint32_t ph = (x / C::kStages) & 1;
+          const int row = tok0 + cur.kv_lo + cur.kt * kBN;
+          ok = wait_bounded(&k_empty[st], ph ^ 1, abort_flag);
           if (!ok) break;
+          mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(sk + st * C::kTileBytes + hf * 16384, &tm_k, &k_full[st],
+                        hf * 64, h, row, pol_kv);
+          ++nk;
+          ok = wait_bounded(&v_empty[st], ph ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(sv + st * C::kTileBytes + hf * 16384, &tm_v, &v_full[st],
+                        hf * 64, h, row, pol_kv);
+          ++nv;
+        }
+        if (!ok) {
+          raise_error(p.hdr, kErrTimeout);
+          *abort_flag = 1;
+        }
+        // Drain: every copy issued into shared memory must land before exit.
+        wait_drain(q_full, 0);
+        for (int st = 0; st < C::kStages; ++st) {
+          if (st < nk) {
+            const int last = st + ((nk - 1 - st) / C::kStages) * C::kStages;
+            wait_drain(&k_full[st], (last / C::kStages) & 1);
+          }
+          if (st < nv) {
+            const int last = st + ((nv - 1 - st) / C::kStages) * C::kStages;
+            wait_drain(&v_full[st], (last / C::kStages) & 1);
+          }
+        }
+      }
+    } else if (warp == 9) {
+      // ------------------------------------------------------- MMA issuer --
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, true);
+        const uint32_t sq = smem_u32(smem + C::kQOff);
+        const uint32_t sk = smem_u32(smem + C::kKOff);
+        const uint32_t sv = smem_u32(smem + C::kVOff);
+
+        auto issue_s = [&](int t, int st) {
+          const uint32_t d = tmem + t * kBN;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
+            mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[t]);
+        };
+        auto issue_pv = [&](int t, int st, bool acc) {
+          const uint32_t d = tmem + C::kOCol + t * D;
+          const uint32_t a = tmem + t * kBN;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t bd =
+                sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
+            mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+
+        Cursor cur;
+        cur.start(ring);
+        int n = 0;
+        {
+          Cursor c2 = cur;
+          for (; c2.s < ring.num_steps; c2.advance(ring)) ++n;
+        }
+        bool ok = wait_bounded(q_full, 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&k_full[0], 0, abort_flag);
+        if (ok && n > 0) {
           tc_fence_after();
-          issue_pv(t, st, !zero_init);
-          if (seg_end) mma_commit(&o_done[t]);
-          if (t == nq - 1) mma_commit(&v_empty[st]);
-          if (has_next) {
-            issue_s(t, st1);
-            if (t == nq - 1) mma_commit(&k_empty[st1]);
-          }
+          for (int t = 0; t < nq; ++t) issue_s(t, 0);
+          mma_commit(&k_empty[0]);
         }
-      }
-      if (!ok) {
-        raise_error(p.hdr, kErrTimeout);
-        *abort_flag = 1;
-      }
-      mma_commit(drain);
-      wait_drain(drain, 0);
-    }
-  } else if (warp < 4 * nq) {
-    // ---------------------------------------------------------- softmax --
-    const int t = warp >> 2;
-    const int r = threadIdx.x & 127;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + t * kBN;
-    const uint32_t o_addr = tmem + lane_base + C::kOCol + t * D;
-    const int q_pos = q0 + t * kBM + r;
-    const bool row_valid = q_pos < ring.q_blk_end;
-    const size_t row_idx = static_cast<size_t>(tok0 + q_pos) * p.num_heads + h;
-    const float c_log2 = p.scale_log2;
-
-    float m_run = kNegInf;  // running max, log2 domain (scaled score * log2 e)
-    float l_run = 0.f;
-    int x = 0;
-    int seg_done = 0;
-    bool ok = true;
-    bool any_pv = false;  // a PV has accumulated into O_t (this segment)
-
-    for (int s = 0; s < ring.num_steps && ok; ++s) {
-      int kv_lo, nt, kv_end;
-      ring.seg(s, kv_lo, nt, kv_end);
-      if (PARTIALS) {
-        if (nt == 0) {
-          if (row_valid) {
-            const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
-            float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
-            for (int q = 0; q < D / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            p.m_steps[so] = kNegInf;
-            p.l_steps[so] = 0.f;
-          }
-          continue;
-        }
-        m_run = kNegInf;
-        l_run = 0.f;
-        any_pv = false;
-      }
-      for (int kt = 0; kt < nt; ++kt, ++x) {
-        ok = __all_sync(0xffffffffu, wait_bounded(&s_full[t], x & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t sr[kBN];
-#pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) tmem_ld32(s_addr + q * 32, sr + q * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) reg_fence32(sr + q * 32);
-
-        // Visible keys of this row form a prefix of the tile.
-        const int kv0 = kv_lo + kt * kBN;
-        const int lim = ring.causal ? min(kv_end, q_pos + 1) : kv_end;
-        const int nvis = lim - kv0;
-        if (nvis < kBN) {
-#pragma unroll
-          for (int cc = 0; cc < kBN; ++cc)
-            if (cc >= nvis) sr[cc] = __float_as_uint(kNegInf);
-        }
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-        for (int cc = 4; cc < kBN; cc += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[cc + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[cc + 3]));
-        }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
-        const float m_new = fmaxf(m_run, m_tile);
-        const bool need = m_new > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = (m_run == kNegInf) ? 0.f : ex2_approx(m_run - m_new);
-          if (any_pv) {
-            // PV of the previous tile completed before S of this tile (same
-            // issuing thread, committed in order), so O_t is stable here.
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-              uint32_t orr[32];
-              tmem_ld32(o_addr + q * 32, orr);
-              tmem_wait_ld();
-              reg_fence32(orr);
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-              tmem_st32(o_addr + q * 32, orr);
+        for (int x = 0; x < n && ok; ++x, cur.advance(ring)) {
+          const int st = x % C::kStages;
+          const uint32_t ph = (x / C::kStages) & 1;
+          // Fused: one accumulation over every ring step.  Partials: O restarts
+          // at each ring step and is read out at its end.
+          const bool zero_init = PARTIALS ? cur.first() : (x == 0);
+          const bool seg_end = PARTIALS ? cur.last() : (x == n - 1);
+          const bool has_next = x + 1 < n;
+          const int st1 = (x + 1) % C::kStages;
+          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+          ok = wait_bounded(&v_full[st], ph, abort_flag);
+          if (ok && has_next) ok = wait_bounded(&k_full[st1], ph1, abort_flag);
+          for (int t = 0; t < nq && ok; ++t) {
+            ok = wait_bounded(&p_full[t], x & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, st, !zero_init);
+            if (seg_end) mma_commit(&o_done[t]);
+            if (t == nq - 1) mma_commit(&v_empty[st]);
+            if (has_next) {
+              issue_s(t, st1);
+              if (t == nq - 1) mma_commit(&k_empty[st1]);
             }
           }
-          l_run *= alpha;
-          m_run = m_new;
         }
-        const float mref = (m_run == kNegInf) ? 0.f : m_run;
-        float l0 = 0.f, l1 = 0.f;
-        uint32_t pk[kBN / 2];
-#pragma unroll
-        for (int k2 = 0; k2 < kBN / 2; ++k2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * k2]), c_log2, -mref));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * k2 + 1]), c_log2, -mref));
-          l0 += p0;
-          l1 += p1;
-          pk[k2] = pack_bf16x2(p0, p1);
+        if (!ok) {
+          raise_error(p.hdr, kErrTimeout);
+          *abort_flag = 1;
         }
-        l_run += l0 + l1;
-        tmem_st32(s_addr, pk);
-        tmem_st32(s_addr + 32, pk + 32);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&p_full[t]);
-        any_pv = true;
-      }
-      if (PARTIALS && ok) {
-        // End of ring step s: write (O_step, m_step, l_step) and restart.
-        ok = __all_sync(0xffffffffu,
-                        wait_bounded(&o_done[t], seg_done & 1, abort_flag));
-        ++seg_done;
-        if (!ok) break;
-        tc_fence_after();
-        const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
-        float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t orr[32];
-          tmem_ld32(o_addr + q * 32, orr);
-          tmem_wait_ld();
-          reg_fence32(orr);
-          if (row_valid) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[q * 8 + e / 4] =
-                  make_float4(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1]),
-                              __uint_as_float(orr[e + 2]), __uint_as_float(orr[e + 3]));
-          }
-        }
-        if (row_valid) {
-          p.m_steps[so] = (m_run == kNegInf) ? kNegInf : m_run * kLn2;
-          p.l_steps[so] = l_run;
-        }
-        tc_fence_before();
+        mma_commit(drain);
+        wait_drain(drain, 0);
       }
     }
-    if (!PARTIALS && ok) {
-      // Epilogue: O / l in bf16 and LSE = m + ln l.
-      ok = __all_sync(0xffffffffu, wait_bounded(&o_done[t], 0, abort_flag));
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + row_idx * D);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t orr[32];
-          tmem_ld32(o_addr + q * 32, orr);
-          tmem_wait_ld();
-          reg_fence32(orr);
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                               __uint_as_float(orr[2 * e + 1]) * inv_l);
-          if (row_valid) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+  } else {
+    regs_raise_224();
+    if (warp < 4 * nq) {
+      // ---------------------------------------------------------- softmax --
+      const int t = warp >> 2;
+      const int r = threadIdx.x & 127;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t s_addr = tmem + lane_base + t * kBN;
+      const uint32_t o_addr = tmem + lane_base + C::kOCol + t * D;
+      const int q_pos = q0 + t * kBM + r;
+      const bool row_valid = q_pos < ring.q_blk_end;
+      const size_t row_idx = static_cast<size_t>(tok0 + q_pos) * p.num_heads + h;
+      const float c_log2 = p.scale_log2;
+
+      float m_run = kNegInf;  // running max, log2 domain (scaled score * log2 e)
+      float l_run = 0.f;
+      int x = 0;
+      int seg_done = 0;
+      bool ok = true;
+      bool any_pv = false;  // a PV has accumulated into O_t (this segment)
+
+      for (int s = 0; s < ring.num_steps && ok; ++s) {
+        int kv_lo, nt, kv_end;
+        ring.seg(s, kv_lo, nt, kv_end);
+        if (PARTIALS) {
+          if (nt == 0) {
+            if (row_valid) {
+              const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
+              float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
+              for (int q = 0; q < D / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+              p.m_steps[so] = kNegInf;
+              p.l_steps[so] = 0.f;
+            }
+            continue;
           }
+          m_run = kNegInf;
+          l_run = 0.f;
+          any_pv = false;
         }
-        if (row_valid && p.lse != nullptr)
-          p.lse[row_idx] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
-        tc_fence_before();
+        for (int kt = 0; kt < nt; ++kt, ++x) {
+          ok = __all_sync(0xffffffffu, wait_bounded(&s_full[t], x & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t sr[kBN];
+#pragma unroll
+          for (int q = 0; q < kBN / 32; ++q) tmem_ld32(s_addr + q * 32, sr + q * 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < kBN / 32; ++q) reg_fence32(sr + q * 32);
+
+          // Visible keys of this row form a prefix of the tile.
+          const int kv0 = kv_lo + kt * kBN;
+          const int lim = ring.causal ? min(kv_end, q_pos + 1) : kv_end;
+          const int nvis = lim - kv0;
+          if (nvis < kBN) {
+#pragma unroll
+            for (int cc = 0; cc < kBN; ++cc)
+              if (cc >= nvis) sr[cc] = __float_as_uint(kNegInf);
+          }
+          // Row max: four chains of 3-input max.
+          float mx0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
+          float mx1 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
+          float mx2 = fmaxf(__uint_as_float(sr[4]), __uint_as_float(sr[5]));
+          float mx3 = fmaxf(__uint_as_float(sr[6]), __uint_as_float(sr[7]));
+#pragma unroll
+          for (int cc = 8; cc < kBN; cc += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(sr[cc + 6]), __uint_as_float(sr[cc + 7]));
+          }
+          const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
+          const float m_new = fmaxf(m_run, m_tile);
+          const bool need = m_new > m_run + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = (m_run == kNegInf) ? 0.f : ex2_approx(m_run - m_new);
+            if (any_pv) {
+              // PV of the previous tile completed before S of this tile (same
+              // issuing thread, committed in order), so O_t is stable here.
+#pragma unroll
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t orr[32];
+                tmem_ld32(o_addr + q * 32, orr);
+                tmem_wait_ld();
+                reg_fence32(orr);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st32(o_addr + q * 32, orr);
+              }
+            }
+            l_run *= alpha;
+            m_run = m_new;
+          }
+          const float mref = (m_run == kNegInf) ? 0.f : m_run;
+          // p = 2^(s * scale * log2 e - m): packed FMA on pairs, one ex2 each.
+          const float2 c2 = make_float2(c_log2, c_log2);
+          const float2 nm2 = make_float2(-mref, -mref);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          uint32_t pk[kBN / 2];
+#pragma unroll
+          for (int k2 = 0; k2 < kBN / 2; ++k2) {
+            const float2 xs = __ffma2_rn(
+                make_float2(__uint_as_float(sr[2 * k2]), __uint_as_float(sr[2 * k2 + 1])), c2, nm2);
+            const float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+            if (k2 & 1) acc1 = __fadd2_rn(acc1, pp); else acc0 = __fadd2_rn(acc0, pp);
+            pk[k2] = pack_bf16x2(pp.x, pp.y);
+          }
+          l_run += (acc0.x + acc1.x) + (acc0.y + acc1.y);
+          tmem_st32(s_addr, pk);
+          tmem_st32(s_addr + 32, pk + 32);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&p_full[t]);
+          any_pv = true;
+        }
+        if (PARTIALS && ok) {
+          // End of ring step s: write (O_step, m_step, l_step) and restart.
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(&o_done[t], seg_done & 1, abort_flag));
+          ++seg_done;
+          if (!ok) break;
+          tc_fence_after();
+          const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
+          float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + q * 32, orr);
+            tmem_wait_ld();
+            reg_fence32(orr);
+            if (row_valid) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                dst[q * 8 + e / 4] =
+                    make_float4(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1]),
+                                __uint_as_float(orr[e + 2]), __uint_as_float(orr[e + 3]));
+            }
+          }
+          if (row_valid) {
+            p.m_steps[so] = (m_run == kNegInf) ? kNegInf : m_run * kLn2;
+            p.l_steps[so] = l_run;
+          }
+          tc_fence_before();
+        }
       }
-    }
-    if (!ok) {
-      raise_error(p.hdr, kErrTimeout);
-      *abort_flag = 1;
+      if (!PARTIALS && ok) {
+        // Epilogue: O / l in bf16 and LSE = m + ln l.
+        ok = __all_sync(0xffffffffu, wait_bounded(&o_done[t], 0, abort_flag));
+        if (ok) {
+          tc_fence_after();
+          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row_idx * D);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + q * 32, orr);
+            tmem_wait_ld();
+            reg_fence32(orr);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                 __uint_as_float(orr[2 * e + 1]) * inv_l);
+            if (row_valid) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
+          if (row_valid && p.lse != nullptr)
+            p.lse[row_idx] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
+          tc_fence_before();
+        }
+      }
+      if (!ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
     }
   }
 
@@ -530,6 +558,13 @@ static cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const FwdParams& p,
                                  long long grid, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, PARTIALS>;
+  // The register split inside the kernel assumes exactly kLaunchRegs per
+  // thread at launch; with any other count the raise could wait forever.
+  static const int regs = [&] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -13,17 +13,26 @@ constexpr int kBM = 128;               // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;               // keys per KV tile
 constexpr int kNQ = 2;                 // Q tiles per CTA, ping-ponged
 constexpr int kRowsPerItem = kBM * kNQ;
-constexpr int kThreads = 384;          // 2 softmax warpgroups + 1 control WG
+constexpr int kThreads = 384;          // 2 softmax warpgroups + control WG
+// Register split (setmaxnreg): the kernel is launched at kLaunchRegs per
+// thread; the control warpgroup drops to kCtrlRegs and the two softmax
+// warpgroups rise to kSoftmaxRegs.  The shares add up to the launch total:
+// 384 * 168 = 256 * 224 + 128 * 56.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kCtrlRegs = 56;
+static_assert(kThreads * kLaunchRegs == 256 * kSoftmaxRegs + 128 * kCtrlRegs,
+              "register split must match the launch allocation");
 constexpr int kMaxCp = 64;
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)                 WsHeader
-//   [256, +4*(B+1))          per-sample prefix of work items
-//   [.., +8*max_items)       work items (int2: sample, (rank << 20) | block)
+//   [256, +4*(B+1))          first CTA of each sample (in schedule order)
+//   [.., +8*max_items)       schedule order of the samples (B ints used)
 //   [.., ...)                unfused mode only: o_steps, m_steps, l_steps
 struct WsHeader {
   int error;    // cpattn_status of the last kernels run on this workspace
-  int n_items;  // work items built by the schedule kernel
+  int n_items;  // CTAs of the attention grid that have work
   int pad[62];
 };
 
@@ -39,14 +48,14 @@ struct SchedParams {
   const int* cu_seqlens;
   const int* cp_size;  // may be null: every sample at CP 1
   int num_seqs;
+  int num_heads;
   long long total_tokens;
   int max_seqlen;
   int max_cp;
-  int causal;
   WsHeader* hdr;
-  int* prefix;
-  int2* items;
-  long long max_items;
+  int* first_cta;      // [B + 1]: first CTA of the sample at each order position
+  int* order;          // [B]: samples by decreasing length
+  long long max_ctas;  // grid size the host launches
 };
 
 struct FwdParams {
@@ -63,7 +72,9 @@ struct FwdParams {
   float* l_steps;
   long long total_tokens;
   WsHeader* hdr;
-  const int2* items;
+  const int* first_cta;
+  const int* order;
+  int num_seqs;
 };
 
 struct MergeParams {

@@ -255,6 +255,22 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute
+// the same one).  The counts are immediates: 224 and 56.
+__device__ __forceinline__ void regs_raise_224() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+}
+__device__ __forceinline__ void regs_lower_56() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.
