@@ -136,6 +136,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def aggregate(dist, torch, ms, flops, device):
+    """Across ranks: the slowest rank's step time and the sum of all ranks'
+    FLOPs (each rank runs its own batch).  Returns (ms_max, flops_total)."""
+    t = torch.tensor([ms, flops], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(t[1])
+
+
+def whole_job_tflops(total_flops, ms_max):
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    return total_flops / (ms_max * 1e-3) / 1e12
+
+
 def dist_setup(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -312,16 +327,10 @@ def main():
     status = cpattn.poll_error(ws)
     if status != cpattn.OK:
         raise RuntimeError("device status after timed steps: %s" % cpattn.status_string(status))
-    ms_max = ms
-    total_flops = flops
+    ms_max, total_flops = ms, flops
     if world > 1:
-        t = torch.tensor([ms, flops], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        ms_max = float(mx[0])
-        total_flops = float(t[1])
-    value = total_flops * args.steps / (ms_max * args.steps * 1e-3) / 1e12
+        ms_max, total_flops = aggregate(dist, torch, ms, flops, dev)
+    value = whole_job_tflops(total_flops, ms_max)
 
     # --- the attention kernel alone (roofline): average launch duration.
     k_ms = time_loop(torch, kernel_only, args.steps, 3, stream)
@@ -362,10 +371,8 @@ def main():
     d2h = T * H * D * 2 + T * H * 4
     e2e_ms_max = e2e_ms
     if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms_max = float(t[0])
-    e2e_value = total_flops / (e2e_ms_max * 1e-3) / 1e12
+        e2e_ms_max, _ = aggregate(dist, torch, e2e_ms, flops, dev)
+    e2e_value = whole_job_tflops(total_flops, e2e_ms_max)
     del hq, hk, hv, dq, dk, dv
 
     extras = {}
