@@ -52,6 +52,38 @@ def _stale():
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def build_fault_injection(force=False):
+    """Test-only variant ``libcpattn_fault.so`` built with
+    ``-DCPATTN_FAULT_INJECT_DROP_P``: the attention kernel's first CTA skips
+    one hand-off so that a bounded device wait runs out.  Used by the failure
+    detection test; never loaded by the package."""
+    lib = os.path.join(PKG, "libcpattn_fault.so")
+    build()
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(LIB):
+        return lib
+    os.makedirs(BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    flags = _flags() + ["-DCPATTN_FAULT_INJECT_DROP_P=1"]
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, "fault_" + src + ".o")
+        r = subprocess.run([nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed on %s:\n%s" % (src, r.stderr))
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = lib + ".tmp"
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs,
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s" % r.stderr)
+    os.replace(tmp, lib)
+    return lib
+
+
 def build(force=False, verbose_ptxas=False, quiet=True):
     """Compile and link ``libcpattn.so`` unless it is up to date."""
     if not force and not _stale():

@@ -472,7 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(s_addr + 32, pk + 32);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&p_full[t]);
+#ifdef CPATTN_FAULT_INJECT_DROP_P
+          // Test-only build: CTA 0 never hands its first P tile of Q tile 0
+          // to the MMA warp, whose bounded wait then runs out (no trap, no
+          // fault).
+          if (!(blockIdx.x == 0 && t == 0 && x == 0))
+#endif
+            mbar_arrive(&p_full[t]);
           any_pv = true;
         }
         if (PARTIALS && ok) {
