@@ -124,6 +124,7 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   sp.hdr = hdr;
   sp.first_cta = reinterpret_cast<int*>(ws + lay.prefix_off);
   sp.order = reinterpret_cast<int*>(ws + lay.items_off);
+  sp.table = reinterpret_cast<CtaWork*>(ws + lay.table_off);
   sp.max_ctas = grid;
   if (launch_schedule(sp, stream) != cudaSuccess) return CPATTN_ERR_CUDA;
   if (a.T == 0 || a.B == 0) return CPATTN_OK;
@@ -135,8 +136,7 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
     return CPATTN_ERR_CUDA;
 
   FwdParams fp;
-  fp.cu_seqlens = a.cu;
-  fp.cp_size = a.cp;
+  fp.table = sp.table;
   fp.num_heads = a.H;
   fp.num_steps = partials ? num_steps : a.max_cp;
   fp.causal = a.causal;
@@ -148,9 +148,6 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   fp.l_steps = l_steps;
   fp.total_tokens = a.T;
   fp.hdr = hdr;
-  fp.first_cta = sp.first_cta;
-  fp.order = sp.order;
-  fp.num_seqs = a.B;
   if (launch_attn(tq, tk, tv, fp, a.D, partials, grid, stream) != cudaSuccess)
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;
@@ -165,6 +162,8 @@ WsLayout ws_layout(int64_t T, int32_t B, int32_t H, int32_t D, int32_t max_cp,
   off = align_up(off + sizeof(int) * (static_cast<size_t>(B) + 1));
   l.items_off = off;
   off = align_up(off + sizeof(int2) * static_cast<size_t>(l.max_items));
+  l.table_off = off;
+  off = align_up(off + sizeof(CtaWork) * static_cast<size_t>(l.max_items) * H);
   l.o_off = l.m_off = l.l_off = 0;
   if (with_partials) {
     const size_t rows = static_cast<size_t>(max_cp) * T * H;

@@ -20,7 +20,12 @@
 //   warps 4-7   softmax for Q tile 1
 //   warp  8     TMA producer (Q once, then K/V tiles through a stage ring)
 //   warp  9     MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle
+//   warp  10    waits on the hand-offs (mbarriers) for the MMA issuer and
+//               releases it through a named barrier: an mbarrier wait in the
+//               issuing thread right after tcgen05.commit stalls until the
+//               queued MMAs drain (measured on GB300: about 300 cycles of
+//               idle tensor pipe per wait)
+//   warp  11    idle
 // The softmax warpgroups take 224 registers per thread and the control
 // warpgroup (warps 8-11) gives its share up, down to 56.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 and O1 at 256 + t*D.
@@ -139,30 +144,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const FwdParams p) {
   using C = Cfg<D>;
-  const int n_ctas = *reinterpret_cast<volatile int*>(&p.hdr->n_items);
+  // The three loads are independent, so they are in flight together.  The
+  // table holds an entry for every CTA of the grid (used or not).
   const int x_cta = static_cast<int>(blockIdx.x);
+  const int n_ctas = __ldcg(&p.hdr->n_items);
+  const int err0 = __ldcg(&p.hdr->error);
+  const CtaWork work = __ldg(&p.table[x_cta]);
   if (x_cta >= n_ctas) return;
   // After one CTA gave up on a wait, the rest of the grid does no work.
-  if (*reinterpret_cast<volatile int*>(&p.hdr->error) == kErrTimeout) return;
+  if (err0 == kErrTimeout) return;
 
   // CTA -> (sample, head, rank, block): see work.cuh for the order.
-  int pos = 0;
-  {
-    int hi = p.num_seqs - 1;
-    while (pos < hi) {
-      const int mid = (pos + hi + 1) >> 1;
-      if (p.first_cta[mid] <= x_cta) pos = mid; else hi = mid - 1;
-    }
-  }
-  const int b = p.order[pos];
-  const SampleGeom geo = sample_geom(p.cu_seqlens, p.cp_size, b);
-  const int n_b = sample_items(geo);
-  const int e_cta = x_cta - p.first_cta[pos];
-  const int h = e_cta / n_b;
-  int rank, blk;
-  item_coords(geo, n_b - 1 - (e_cta - h * n_b), rank, blk);
-
-  const int tok0 = p.cu_seqlens[b];
+  SampleGeom geo;
+  geo.L = work.y;
+  geo.c = work.z & 0xff;
+  geo.chunk = cdiv(geo.L, geo.c);
+  const int h = static_cast<int>(static_cast<unsigned>(work.z) >> 8);
+  const int rank = work.w & 0xff;
+  const int blk = static_cast<int>(static_cast<unsigned>(work.w) >> 8);
+  const int tok0 = work.x;
   Ring ring;
   ring.L = geo.L;
   ring.c = geo.c;
@@ -195,7 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
+  // The producer thread sets up the barriers and starts the copies of Q and
+  // of the first K/V tile before the CTA-wide barrier, so that their latency
+  // overlaps the TMEM allocation and the barrier.
+  if (warp == 8 && lane == 0) {
     mbar_init(q_full, 1);
     for (int st = 0; st < C::kStages; ++st) {
       mbar_init(&k_full[st], 1);
@@ -211,6 +214,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
+    for (int t = 0; t < nq; ++t)
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
+                    hf * 64, h, tok0 + q0 + t * kBM, pol_q);
+    Cursor cur;
+    cur.start(ring);
+    if (cur.s < ring.num_steps) {  // tile 0 goes to stage 0, which is free
+      const int row = tok0 + cur.kv_lo;
+      mbar_arrive_expect_tx(&k_full[0], C::kTileBytes);
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(smem + C::kKOff + hf * 16384, &tm_k, &k_full[0], hf * 64, h, row,
+                    pol_kv);
+      mbar_arrive_expect_tx(&v_full[0], C::kTileBytes);
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(smem + C::kVOff + hf * 16384, &tm_v, &v_full[0], hf * 64, h, row,
+                    pol_kv);
+    }
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -227,22 +253,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // ------------------------------------------------------ TMA producer --
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        const uint64_t pol_q = l2_policy_evict_first();
         const uint64_t pol_kv = l2_policy_evict_last();
-        uint8_t* sq = smem + C::kQOff;
         uint8_t* sk = smem + C::kKOff;
         uint8_t* sv = smem + C::kVOff;
-        mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
-        for (int t = 0; t < nq; ++t)
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(sq + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
-                        hf * 64, h, tok0 + q0 + t * kBM, pol_q);
+        // Q and tile 0 were issued before the CTA barrier.
         Cursor cur;
         cur.start(ring);
         int nk = 0, nv = 0;  // K and V tiles whose copies were issued
+        if (cur.s < ring.num_steps) {
+          nk = nv = 1;
+          cur.advance(ring);
+        }
         bool ok = true;
         for (; cur.s < ring.num_steps; cur.advance(ring)) {
           const int x = nk;
@@ -283,64 +304,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 9) {
       // ------------------------------------------------------- MMA issuer --
-      if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, true);
-        const uint32_t sq = smem_u32(smem + C::kQOff);
-        const uint32_t sk = smem_u32(smem + C::kKOff);
-        const uint32_t sv = smem_u32(smem + C::kVOff);
+      // Lane 0 issues every MMA and never touches an mbarrier in the loop: a
+      // wait right after a commit stalls the tensor queue.  Warp 10 does the
+      // waiting and releases this warp through named barrier 1 before each
+      // block of MMAs (both warps run the same number of rendezvous).
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, true);
+      const uint32_t sq = smem_u32(smem + C::kQOff);
+      const uint32_t sk = smem_u32(smem + C::kKOff);
+      const uint32_t sv = smem_u32(smem + C::kVOff);
 
-        auto issue_s = [&](int t, int st) {
-          const uint32_t d = tmem + t * kBN;
+      auto issue_s = [&](int t, int st) {
+        const uint32_t d = tmem + t * kBN;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
-            mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_full[t]);
-        };
-        auto issue_pv = [&](int t, int st, bool acc) {
-          const uint32_t d = tmem + C::kOCol + t * D;
-          const uint32_t a = tmem + t * kBN;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
+          mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int st, bool acc) {
+        const uint32_t d = tmem + C::kOCol + t * D;
+        const uint32_t a = tmem + t * kBN;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t bd =
-                sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
-            mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
-          }
-        };
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
+          mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
 
-        Cursor cur;
-        cur.start(ring);
-        int n = 0;
-        {
-          Cursor c2 = cur;
-          for (; c2.s < ring.num_steps; c2.advance(ring)) ++n;
-        }
-        bool ok = wait_bounded(q_full, 0, abort_flag);
-        if (ok && n > 0) ok = wait_bounded(&k_full[0], 0, abort_flag);
-        if (ok && n > 0) {
-          tc_fence_after();
-          for (int t = 0; t < nq; ++t) issue_s(t, 0);
-          mma_commit(&k_empty[0]);
-        }
-        for (int x = 0; x < n && ok; ++x, cur.advance(ring)) {
-          const int st = x % C::kStages;
-          const uint32_t ph = (x / C::kStages) & 1;
-          // Fused: one accumulation over every ring step.  Partials: O restarts
-          // at each ring step and is read out at its end.
-          const bool zero_init = PARTIALS ? cur.first() : (x == 0);
-          const bool seg_end = PARTIALS ? cur.last() : (x == n - 1);
-          const bool has_next = x + 1 < n;
-          const int st1 = (x + 1) % C::kStages;
-          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-          ok = wait_bounded(&v_full[st], ph, abort_flag);
-          if (ok && has_next) ok = wait_bounded(&k_full[st1], ph1, abort_flag);
-          for (int t = 0; t < nq && ok; ++t) {
-            ok = wait_bounded(&p_full[t], x & 1, abort_flag);
-            if (!ok) break;
+      Cursor cur;
+      cur.start(ring);
+      int n = 0;
+      {
+        Cursor c2 = cur;
+        for (; c2.s < ring.num_steps; c2.advance(ring)) ++n;
+      }
+      named_bar_sync(1, 64);  // Q and K(0) landed
+      if (lane == 0 && n > 0) {
+        tc_fence_after();
+        for (int t = 0; t < nq; ++t) issue_s(t, 0);
+        mma_commit(&k_empty[0]);
+      }
+      __syncwarp();
+      for (int x = 0; x < n; ++x, cur.advance(ring)) {
+        const int st = x % C::kStages;
+        // Fused: one accumulation over every ring step.  Partials: O restarts
+        // at each ring step and is read out at its end.
+        const bool zero_init = PARTIALS ? cur.first() : (x == 0);
+        const bool seg_end = PARTIALS ? cur.last() : (x == n - 1);
+        const bool has_next = x + 1 < n;
+        const int st1 = (x + 1) % C::kStages;
+        for (int t = 0; t < nq; ++t) {
+          named_bar_sync(1, 64);  // P_t(x), V(x) and K(x+1) are ready
+          if (lane == 0) {
             tc_fence_after();
             issue_pv(t, st, !zero_init);
             if (seg_end) mma_commit(&o_done[t]);
@@ -350,14 +370,51 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (t == nq - 1) mma_commit(&k_empty[st1]);
             }
           }
+          __syncwarp();
         }
-        if (!ok) {
-          raise_error(p.hdr, kErrTimeout);
-          *abort_flag = 1;
-        }
+      }
+      if (lane == 0) {
         mma_commit(drain);
         wait_drain(drain, 0);
       }
+      __syncwarp();
+    } else if (warp == 10) {
+      // ------------------------------------------------ waits for the MMAs --
+      // After a failed (bounded) wait the remaining rendezvous still happen,
+      // without waiting, so the MMA warp always runs to its end.
+      Cursor cur;
+      cur.start(ring);
+      int n = 0;
+      for (; cur.s < ring.num_steps; cur.advance(ring)) ++n;
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_bounded(q_full, 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&k_full[0], 0, abort_flag);
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);
+      for (int x = 0; x < n; ++x) {
+        const int st = x % C::kStages;
+        const uint32_t ph = (x / C::kStages) & 1;
+        const int st1 = (x + 1) % C::kStages;
+        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+        for (int t = 0; t < nq; ++t) {
+          if (lane == 0 && ok) {
+            if (t == 0) {
+              ok = wait_bounded(&v_full[st], ph, abort_flag);
+              if (ok && x + 1 < n) ok = wait_bounded(&k_full[st1], ph1, abort_flag);
+            }
+            if (ok) ok = wait_bounded(&p_full[t], x & 1, abort_flag);
+          }
+          __syncwarp();
+          named_bar_sync(1, 64);
+        }
+      }
+      if (lane == 0 && !ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
+      __syncwarp();
     }
   } else {
     regs_raise_224();

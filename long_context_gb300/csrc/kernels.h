@@ -29,6 +29,7 @@ constexpr int kMaxCp = 64;
 //   [0, 256)                 WsHeader
 //   [256, +4*(B+1))          first CTA of each sample (in schedule order)
 //   [.., +8*max_items)       schedule order of the samples (B ints used)
+//   [.., +16*max_items*H)    work table: one CtaWork per attention CTA
 //   [.., ...)                unfused mode only: o_steps, m_steps, l_steps
 struct WsHeader {
   int error;    // cpattn_status of the last kernels run on this workspace
@@ -37,9 +38,16 @@ struct WsHeader {
 };
 
 struct WsLayout {
-  size_t prefix_off, items_off, o_off, m_off, l_off, total;
+  size_t prefix_off, items_off, table_off, o_off, m_off, l_off, total;
   int64_t max_items;
 };
+
+// One attention CTA's work, written by the schedule kernel so that a CTA
+// finds it with a single 16-byte load:
+//   x = first token of the sample, y = sample length L,
+//   z = (head << 8) | CP size c,  w = (query block << 8) | CP rank.
+// (head < 2^16, c <= 64, rank < c, block < 2^23 since L < 2^31.)
+using CtaWork = int4;
 
 WsLayout ws_layout(int64_t T, int32_t B, int32_t H, int32_t D, int32_t max_cp,
                    bool with_partials);
@@ -55,12 +63,12 @@ struct SchedParams {
   WsHeader* hdr;
   int* first_cta;      // [B + 1]: first CTA of the sample at each order position
   int* order;          // [B]: samples by decreasing length
+  CtaWork* table;      // [max_ctas]: work of each CTA (first n_items used)
   long long max_ctas;  // grid size the host launches
 };
 
 struct FwdParams {
-  const int* cu_seqlens;
-  const int* cp_size;
+  const CtaWork* table;  // [grid]: written by the schedule kernel
   int num_heads;
   int num_steps;        // ring steps walked: max_cp (fused) or S (partials)
   int causal;
@@ -72,9 +80,6 @@ struct FwdParams {
   float* l_steps;
   long long total_tokens;
   WsHeader* hdr;
-  const int* first_cta;
-  const int* order;
-  int num_seqs;
 };
 
 struct MergeParams {

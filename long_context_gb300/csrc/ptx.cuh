@@ -76,6 +76,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Named barrier `id` over `n` threads (whole warps; every lane of each
+// participating warp executes it).  Not a memory access.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

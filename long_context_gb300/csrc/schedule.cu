@@ -5,9 +5,10 @@
 // head) -- "Dynamic Context Parallelism (DCP)": each sample has its own CP
 // size; "Megatron 架构与 6D 并行完整指南" section 六: rank i owns chunk i.
 // Order (see work.cuh): samples by decreasing length, then head, then block
-// by decreasing cost.  This kernel writes the sample order and, for each
-// position in it, the first CTA index of that sample; the attention kernel
-// finds its sample by binary search and derives head and block from the rest.
+// by decreasing cost.  This kernel writes the sample order, for each position
+// in it the first CTA index of that sample, and then the work of every CTA
+// (sample start and length, CP size, head, rank, block) into a table that the
+// attention kernel reads with one load per CTA.
 #include "kernels.h"
 #include "work.cuh"
 
@@ -123,11 +124,48 @@ __global__ void __launch_bounds__(kSchedThreads)
     if (tid == 0) p.hdr->error = 1;
     return;
   }
-  if (tid == 0) {
-    p.first_cta[p.num_seqs] = static_cast<int>(total);
-    __threadfence();
-    p.hdr->n_items = static_cast<int>(total);
+  if (tid == 0) p.first_cta[p.num_seqs] = static_cast<int>(total);
+  __syncthreads();
+
+  // Work table: each thread fills a contiguous run of CTA indices, finding
+  // the sample position of the first one by binary search and walking on.
+  const int n_ctas = static_cast<int>(total);
+  const int per = (n_ctas + kSchedThreads - 1) / kSchedThreads;
+  const int x_begin = min(tid * per, n_ctas);
+  const int x_end = min(x_begin + per, n_ctas);
+  if (x_begin < x_end) {
+    int pos = 0;
+    {
+      int hi = p.num_seqs - 1;
+      while (pos < hi) {
+        const int mid = (pos + hi + 1) >> 1;
+        if (p.first_cta[mid] <= x_begin) pos = mid; else hi = mid - 1;
+      }
+    }
+    int next = p.first_cta[pos + 1];
+    int b = p.order[pos];
+    SampleGeom g = sample_geom(p.cu_seqlens, p.cp_size, b);
+    int n_b = sample_items(g);
+    int first = p.first_cta[pos];
+    for (int x = x_begin; x < x_end; ++x) {
+      while (x >= next) {  // samples without CTAs (L = 0) are passed over
+        ++pos;
+        first = next;
+        next = p.first_cta[pos + 1];
+        b = p.order[pos];
+        g = sample_geom(p.cu_seqlens, p.cp_size, b);
+        n_b = sample_items(g);
+      }
+      const int e = x - first;
+      const int h = e / n_b;
+      int rank, blk;
+      item_coords(g, n_b - 1 - (e - h * n_b), rank, blk);
+      p.table[x] = make_int4(p.cu_seqlens[b], g.L, (h << 8) | g.c,
+                             static_cast<int>((static_cast<unsigned>(blk) << 8) |
+                                              static_cast<unsigned>(rank)));
+    }
   }
+  if (tid == 0) p.hdr->n_items = n_ctas;
 }
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream) {
