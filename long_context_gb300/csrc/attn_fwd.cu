@@ -47,6 +47,10 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // this many powers of two; until then exp2 values stay below 2^8.  O and l
 // share the stale reference, so O / l and m + ln l are unchanged.
 constexpr float kRescaleThreshold = 8.0f;
+// A tile whose exponentials, taken against the running max as it stands,
+// sum above this bound is redone with its own row max (so every P value
+// stays below 2^16).
+constexpr float kMaxLazyTileSum = 65536.0f;
 
 enum : int {
   kErrInvalid = 1,
@@ -314,26 +318,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sk = smem_u32(smem + C::kKOff);
       const uint32_t sv = smem_u32(smem + C::kVOff);
 
+      // Descriptor words: the high word is constant; the low word holds the
+      // start address >> 4 (14 bits, shared memory is below 2^18 bytes) and
+      // the leading byte offset, so tile and k-step offsets are 32-bit adds.
+      const uint32_t hi_kq = static_cast<uint32_t>(sdesc_sw128(0, 16, 1024) >> 32);
+      const uint32_t hi_v = static_cast<uint32_t>(sdesc_sw128(0, 16384, 1024) >> 32);
+      const uint32_t lo_q = static_cast<uint32_t>(sdesc_sw128(sq, 16, 1024));
+      const uint32_t lo_k = static_cast<uint32_t>(sdesc_sw128(sk, 16, 1024));
+      const uint32_t lo_v = static_cast<uint32_t>(sdesc_sw128(sv, 16384, 1024));
       auto issue_s = [&](int t, int st) {
         const uint32_t d = tmem + t * kBN;
+        const uint32_t a0 = lo_q + t * (C::kTileBytes >> 4);
+        const uint32_t b0 = lo_k + st * (C::kTileBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
-          mma_ss(d, a, bd, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(d, pack_u64(a0 + off, hi_kq), pack_u64(b0 + off, hi_kq), idesc_s,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int st, bool acc) {
         const uint32_t d = tmem + C::kOCol + t * D;
         const uint32_t a = tmem + t * kBN;
+        const uint32_t b0 = lo_v + st * (C::kTileBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(sv + st * C::kTileBytes + kk * 2048, 16384, 1024);
-          mma_ts(d, a + kk * 8, bd, idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(d, a + kk * 8, pack_u64(b0 + ((kk * 2048) >> 4), hi_v), idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
       };
 
       Cursor cur;
@@ -459,6 +471,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bounded(&s_full[t], x & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
+          // The row max is taken only when the warp has a row without a
+          // reference yet; otherwise the exponentials use the running max as
+          // it is, and the tile is redone with its own max only if that
+          // reference was too low (a tile sum above 2^16, or not finite).  S
+          // is still in TMEM for the redo, since P has not been written yet.
+          bool with_max = __any_sync(0xffffffffu, m_run == kNegInf);
+          float2 acc0, acc1;
+          uint32_t pk[kBN / 2];
+#pragma unroll 1
+          for (;;) {
           uint32_t sr[kBN];
 #pragma unroll
           for (int q = 0; q < kBN / 32; ++q) tmem_ld32(s_addr + q * 32, sr + q * 32);
@@ -475,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < kBN; ++cc)
               if (cc >= nvis) sr[cc] = __float_as_uint(kNegInf);
           }
+          if (with_max) {
           // Row max: four chains of 3-input max.
           float mx0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
           float mx1 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
@@ -510,12 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run *= alpha;
             m_run = m_new;
           }
+          }
           const float mref = (m_run == kNegInf) ? 0.f : m_run;
           // p = 2^(s * scale * log2 e - m): packed FMA on pairs, one ex2 each.
           const float2 c2 = make_float2(c_log2, c_log2);
           const float2 nm2 = make_float2(-mref, -mref);
-          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-          uint32_t pk[kBN / 2];
+          acc0 = make_float2(0.f, 0.f);
+          acc1 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int k2 = 0; k2 < kBN / 2; ++k2) {
             const float2 xs = __ffma2_rn(
@@ -523,6 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
             if (k2 & 1) acc1 = __fadd2_rn(acc1, pp); else acc0 = __fadd2_rn(acc0, pp);
             pk[k2] = pack_bf16x2(pp.x, pp.y);
+          }
+          if (with_max) break;
+          const float l_tile = (acc0.x + acc1.x) + (acc0.y + acc1.y);
+          if (!__any_sync(0xffffffffu, !(l_tile <= kMaxLazyTileSum))) break;
+          with_max = true;
           }
           l_run += (acc0.x + acc1.x) + (acc0.y + acc1.y);
           tmem_st32(s_addr, pk);

@@ -57,22 +57,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete sleeps until it
+// completes or `sleep_ns` pass, instead of returning at once: waiting warps
+// then take no issue slots from the warps that share their sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t sleep_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Give up after this long: no legitimate wait inside one CTA comes close.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Longest single sleep inside wait_bounded (bounds how late an abort raised
+// by another warp is seen).
+constexpr uint32_t kWaitSleepNs = 20000;  // 20 us
 
 // Wait until the phase with the given parity of `bar` has completed.
 // Returns false when the wait gave up, either because *abort was raised by
 // another warp of the CTA or because kWaitLimitNs passed.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 
@@ -193,6 +210,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N,
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 family layout:
 //   bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
 //   offset >> 4, 46-47 version (1), 61-63 layout (2 = 128-byte swizzle).
+// A 64-bit value from two 32-bit halves (a register pair, no arithmetic).
+__device__ __forceinline__ uint64_t pack_u64(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr,
                                                 uint32_t lbo_bytes,
                                                 uint32_t sbo_bytes) {

@@ -116,6 +116,26 @@ def test_large_scores_and_rescale(cp):
     check_attention(out, lse, ref_o, ref_lse, "large scores")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_late_dominant_keys(cp, causal):
+    """Keys from token 512 on have 6x larger components, so for every row that
+    sees them the scores jump by many powers of two after the first KV tiles:
+    the running max found on the early tiles is far too low for the late ones
+    and those tiles must be taken again with their own max."""
+    lengths = [1000, 900]
+    H, D = 2, 128
+    (q, k, v, cu), g = make_batch(lengths, H, D, seed=21)
+    k = k.clone()
+    for b in range(len(lengths)):
+        k[int(cu[b]) + 512:int(cu[b + 1])] *= 6
+    g["k"] = k.to("cuda")
+    scale = default_scale(D)
+    out, lse = _run(cp, g, lengths, [1, 2], H, D, causal, 0, scale)
+    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+    ref_o, ref_lse = oa.full_attention(qf, kf, vf, cu, scale, causal=causal)
+    check_attention(out, lse, ref_o, ref_lse, "late dominant keys")
+
+
 def test_cp_invariance(cp):
     """Only the CP assignment changes: static CP 1/2/4/8 and the dynamic plan
     all agree with the oracle (and the dynamic plan matches the oracle's)."""
