@@ -32,6 +32,8 @@ Modules:
   stored per-step partials, and row-sampled attention for large inputs.
 * :mod:`oracle.planner`   -- the dynamic-CP planner (CP size per sample and
   aligned-group first-fit packing into micro-batches) plus brute-force checkers.
+* :mod:`oracle.backward`  -- the attention backward (dQ, dK, dV): the exact
+  derivative of the forward's definition, in full and over the ring's blocks.
 """
 
-from . import attention, planner  # noqa: F401
+from . import attention, backward, planner  # noqa: F401
