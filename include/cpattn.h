@@ -212,6 +212,57 @@ int cpattn_merge(const float* o_steps, const float* m_steps,
                  float* out_m, float* out_l, void* stream);
 
 /*
+ * cpattn_bwd_workspace_size -- bytes of device workspace cpattn_bwd needs for
+ * a problem of this size (0 on invalid arguments).  The workspace holds the
+ * error word, the schedule, one 16-byte work entry per backward CTA (two
+ * tables) and D = rowsum(dO * O) as float32 [T, H].
+ */
+size_t cpattn_bwd_workspace_size(int64_t total_tokens, int32_t num_seqs,
+                                 int32_t num_heads, int32_t head_dim,
+                                 int32_t max_cp);
+
+/*
+ * cpattn_bwd -- gradients dQ, dK, dV of cpattn_fwd's output O with respect to
+ * Q, K and V, for an upstream gradient dO.
+ *
+ * The pages run a backward pass after the forward in every training step
+ * ("20-Megatron-MCore-TP-PP-EP如何支撑MoE", section 4, forward_backward_batch;
+ * "VeRL Backend Parallelism", MindSpeed-MM recipe, loss.backward()) but give no
+ * formula; this is the exact derivative of the forward's definition ("Megatron
+ * 架构与 6D 并行完整指南", section 六).  With P = exp(scale * Q K^T - LSE) over
+ * the visible pairs of each sample:
+ *   dV = P^T dO,  D = rowsum(dO * O),  dS = P * (dO V^T - D),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q.
+ * The work follows the ring's chunks of each sample (cp_size): dQ of a query
+ * block walks the KV chunks in the forward's ring order; dK, dV of a key block
+ * walk the query chunks that see it in the order they visit it.
+ *
+ * Arguments (device pointers unless stated; everything enqueued on `stream`):
+ *   q, k, v, cu_seqlens, cp_size, num_seqs, total_tokens, max_seqlen, max_cp,
+ *   num_heads, head_dim, softmax_scale, causal
+ *          exactly as passed to the cpattn_fwd call being differentiated.
+ *   out    bf16 [T, H, D]: that call's O (16-byte aligned).
+ *   dout   bf16 [T, H, D]: dO (16-byte aligned).
+ *   lse    float32 [T, H]: that call's LSE (natural log).
+ *   dq, dk, dv  bf16 [T, H, D] outputs (16-byte aligned; every row of every
+ *          sample is written).
+ *   workspace, workspace_bytes  at least cpattn_bwd_workspace_size(...) bytes,
+ *          256-byte aligned, caller-owned.
+ * Precision: fp32 accumulation on the tensor cores; P and dS are rounded to
+ * bf16 before their products; outputs are rounded to bf16.
+ * Errors: argument problems return CPATTN_ERR_INVALID_ARG /
+ * CPATTN_ERR_UNSUPPORTED / CPATTN_ERR_WORKSPACE_TOO_SMALL before anything is
+ * enqueued; device-side problems are reported by cpattn_poll_error.
+ */
+int cpattn_bwd(const void* q, const void* k, const void* v, const void* out,
+               const void* dout, const float* lse, const int32_t* cu_seqlens,
+               const int32_t* cp_size, int32_t num_seqs, int64_t total_tokens,
+               int32_t max_seqlen, int32_t max_cp, int32_t num_heads,
+               int32_t head_dim, float softmax_scale, int32_t causal, void* dq,
+               void* dk, void* dv, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/*
  * cpattn_fwd_noalloc -- cpattn_fwd (CPATTN_MODE_FUSED) for callers that cannot
  * allocate device memory.
  *

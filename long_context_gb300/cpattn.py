@@ -56,6 +56,12 @@ _lib.cpattn_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _
 _lib.cpattn_fwd_noalloc.restype = ctypes.c_int
 _lib.cpattn_merge.argtypes = [_vp, _vp, _vp, _i32, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
 _lib.cpattn_merge.restype = ctypes.c_int
+_lib.cpattn_bwd_workspace_size.argtypes = [_i64, _i32, _i32, _i32, _i32]
+_lib.cpattn_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.cpattn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                            _i32, _i32, ctypes.c_float, _i32, _vp, _vp, _vp, _vp,
+                            ctypes.c_size_t, _vp]
+_lib.cpattn_bwd.restype = ctypes.c_int
 _lib.cpattn_poll_error.argtypes = [_vp, _vp]
 _lib.cpattn_poll_error.restype = ctypes.c_int
 _lib.cpattn_status_string.argtypes = [ctypes.c_int]
@@ -262,6 +268,59 @@ def fwd_partials(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp, num_s
                                   workspace.numel(), _stream(stream))
     _check(st, "cpattn_fwd_partials")
     return o_steps, m_steps, l_steps
+
+
+# --------------------------------------------------------------- backward --
+
+def bwd_workspace_size(total_tokens, num_seqs, num_heads, head_dim, max_cp):
+    n = _lib.cpattn_bwd_workspace_size(int(total_tokens), int(num_seqs), int(num_heads),
+                                       int(head_dim), int(max_cp))
+    if n == 0:
+        raise CpattnError(ERR_INVALID_ARG, "cpattn_bwd_workspace_size")
+    return int(n)
+
+
+def alloc_bwd_workspace(total_tokens, num_seqs, num_heads, head_dim, max_cp, device=None):
+    """A device workspace sized for ``cpattn_bwd`` (torch-owned)."""
+    n = bwd_workspace_size(total_tokens, num_seqs, num_heads, head_dim, max_cp)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def bwd(q, k, v, out, dout, lse, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
+        softmax_scale=None, causal=True, dq=None, dk=None, dv=None, workspace=None,
+        stream=None):
+    """Ring-attention backward (``cpattn_bwd``); returns ``(dq, dk, dv)``.
+
+    ``out`` and ``lse`` are the outputs of the :func:`fwd` call being
+    differentiated (same ``q, k, v, cu_seqlens, cp_size``, scale and causal
+    flag); ``dout`` is the upstream gradient, bf16 ``[T, H, D]``.
+    """
+    dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
+    T, H, D = q.shape
+    B = cu_seqlens.numel() - 1
+    _need(out, "out", torch.bfloat16, dev, q.shape)
+    _need(dout, "dout", torch.bfloat16, dev, q.shape)
+    _need(lse, "lse", torch.float32, dev, (T, H))
+    if max_cp is None:
+        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    grads = []
+    for name, g in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if g is None:
+            g = torch.empty_like(q)
+        else:
+            _need(g, name, torch.bfloat16, dev, q.shape)
+        grads.append(g)
+    if workspace is None:
+        workspace = alloc_bwd_workspace(T, B, H, D, max_cp, dev)
+    st = _lib.cpattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                         _ptr(cu_seqlens), _ptr(cp_size), B, T, int(max_seqlen), int(max_cp),
+                         H, D, float(softmax_scale), 1 if causal else 0, _ptr(grads[0]),
+                         _ptr(grads[1]), _ptr(grads[2]), _ptr(workspace), workspace.numel(),
+                         _stream(stream))
+    _check(st, "cpattn_bwd")
+    return tuple(grads)
 
 
 def merge(o_steps, m_steps, l_steps, *, out_o=None, out_m=None, out_l=None, stream=None):

@@ -125,7 +125,9 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   sp.first_cta = reinterpret_cast<int*>(ws + lay.prefix_off);
   sp.order = reinterpret_cast<int*>(ws + lay.items_off);
   sp.table = reinterpret_cast<CtaWork*>(ws + lay.table_off);
+  sp.table_asc = nullptr;
   sp.max_ctas = grid;
+  sp.rows_per_item = kRowsPerItem;
   if (launch_schedule(sp, stream) != cudaSuccess) return CPATTN_ERR_CUDA;
   if (a.T == 0 || a.B == 0) return CPATTN_OK;
 
@@ -298,6 +300,127 @@ extern "C" int cpattn_merge(const float* o_steps, const float* m_steps,
   mp.out_l = out_l;
   if (launch_merge(mp, head_dim, false, dev.num_sms,
                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  return CPATTN_OK;
+}
+
+// ------------------------------------------------------------- backward --
+
+namespace cpattn {
+namespace {
+
+constexpr int kBwdRows = 128;  // rows per backward work unit (one tile)
+
+struct BwdLayout {
+  size_t prefix_off, order_off, table_dq_off, table_kv_off, delta_off, total;
+  int64_t max_items;
+};
+
+BwdLayout bwd_layout(int64_t T, int32_t B, int32_t H, int32_t max_cp) {
+  BwdLayout l;
+  l.max_items = T / kBwdRows + static_cast<int64_t>(B) * max_cp + 1;
+  size_t off = align_up(sizeof(WsHeader));
+  l.prefix_off = off;
+  off = align_up(off + sizeof(int) * (static_cast<size_t>(B) + 1));
+  l.order_off = off;
+  off = align_up(off + sizeof(int) * (static_cast<size_t>(B) + 1));
+  l.table_dq_off = off;
+  off = align_up(off + sizeof(CtaWork) * static_cast<size_t>(l.max_items) * H);
+  l.table_kv_off = off;
+  off = align_up(off + sizeof(CtaWork) * static_cast<size_t>(l.max_items) * H);
+  l.delta_off = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(T) * H);
+  l.total = off;
+  return l;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+extern "C" size_t cpattn_bwd_workspace_size(int64_t total_tokens, int32_t num_seqs,
+                                            int32_t num_heads, int32_t head_dim,
+                                            int32_t max_cp) {
+  if (total_tokens < 0 || num_seqs < 0 || num_heads < 1 || max_cp < 1 ||
+      max_cp > kMaxCp || (head_dim != 64 && head_dim != 128))
+    return 0;
+  return bwd_layout(total_tokens, num_seqs, num_heads, max_cp).total;
+}
+
+extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, const int32_t* cu_seqlens,
+                          const int32_t* cp_size, int32_t num_seqs, int64_t total_tokens,
+                          int32_t max_seqlen, int32_t max_cp, int32_t num_heads,
+                          int32_t head_dim, float softmax_scale, int32_t causal, void* dq,
+                          void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  FwdArgs a{q, k, v, cu_seqlens, cp_size, num_seqs, total_tokens, max_seqlen,
+            max_cp, num_heads, head_dim, softmax_scale, causal};
+  int st = check_fwd(a);
+  if (st != CPATTN_OK) return st;
+  if (total_tokens > 0) {
+    for (const void* ptr : {out, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                            static_cast<const void*>(dv)})
+      if (ptr == nullptr || !aligned(ptr, 16)) return CPATTN_ERR_INVALID_ARG;
+    if (lse == nullptr || !aligned(lse, 4)) return CPATTN_ERR_INVALID_ARG;
+  }
+  if (workspace == nullptr || !aligned(workspace, kAlign)) return CPATTN_ERR_INVALID_ARG;
+  const BwdLayout lay = bwd_layout(total_tokens, num_seqs, num_heads, max_cp);
+  if (workspace_bytes < lay.total) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  st = device_info(&dev);
+  if (st != CPATTN_OK) return st;
+  if (dev.cc_major != 10 || dev.cc_minor != 3) return CPATTN_ERR_UNSUPPORTED;
+  const long long grid = lay.max_items * num_heads;
+  if (grid > 0x7fffffffLL) return CPATTN_ERR_UNSUPPORTED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* delta = reinterpret_cast<float*>(ws + lay.delta_off);
+  if (launch_bwd_delta(static_cast<const __nv_bfloat16*>(out),
+                       static_cast<const __nv_bfloat16*>(dout), delta,
+                       total_tokens * num_heads, head_dim, dev.num_sms, s) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  SchedParams sp;
+  sp.cu_seqlens = cu_seqlens;
+  sp.cp_size = cp_size;
+  sp.num_seqs = num_seqs;
+  sp.num_heads = num_heads;
+  sp.total_tokens = total_tokens;
+  sp.max_seqlen = max_seqlen;
+  sp.max_cp = max_cp;
+  sp.hdr = hdr;
+  sp.first_cta = reinterpret_cast<int*>(ws + lay.prefix_off);
+  sp.order = reinterpret_cast<int*>(ws + lay.order_off);
+  sp.table = reinterpret_cast<CtaWork*>(ws + lay.table_dq_off);     // query blocks, costly first
+  sp.table_asc = reinterpret_cast<CtaWork*>(ws + lay.table_kv_off); // key blocks, costly first
+  sp.max_ctas = grid;
+  sp.rows_per_item = kBwdRows;
+  if (launch_schedule(sp, s) != cudaSuccess) return CPATTN_ERR_CUDA;
+  if (total_tokens == 0 || num_seqs == 0) return CPATTN_OK;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_qkv_map(&tq, q, total_tokens, num_heads, head_dim) != CPATTN_OK ||
+      make_qkv_map(&tk, k, total_tokens, num_heads, head_dim) != CPATTN_OK ||
+      make_qkv_map(&tv, v, total_tokens, num_heads, head_dim) != CPATTN_OK ||
+      make_qkv_map(&tdo, dout, total_tokens, num_heads, head_dim) != CPATTN_OK)
+    return CPATTN_ERR_CUDA;
+  BwdParams bp;
+  bp.lse = lse;
+  bp.delta = delta;
+  bp.dq = static_cast<__nv_bfloat16*>(dq);
+  bp.dk = static_cast<__nv_bfloat16*>(dk);
+  bp.dv = static_cast<__nv_bfloat16*>(dv);
+  bp.num_heads = num_heads;
+  bp.causal = causal;
+  bp.scale = softmax_scale;
+  bp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  bp.hdr = hdr;
+  bp.table = sp.table_asc;
+  if (launch_bwd_dkdv(tq, tk, tv, tdo, bp, head_dim, grid, s) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  bp.table = sp.table;
+  if (launch_bwd_dq(tq, tk, tv, tdo, bp, head_dim, grid, s) != cudaSuccess)
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;
 }

@@ -1,0 +1,878 @@
+// Ring-attention backward for sm_103a: dQ, dK, dV of the forward in
+// attn_fwd.cu, on the tensor cores (tcgen05, accumulators in TMEM, tiles
+// staged by TMA).
+//
+// The gradient is the exact derivative of the forward's definition ("Megatron
+// 架构与 6D 并行完整指南", section 六: every query attends to every visible
+// key).  With P = exp(scale * Q K^T - LSE) over visible pairs and an upstream
+// dO:
+//   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+// LSE comes from the forward, so P needs no running max here.  The work is
+// split by the ring's chunks as in the forward: the dQ kernel walks the KV
+// chunks of its query block in the forward's ring order, and the dK/dV kernel
+// walks the query chunks that see its key block in the order they visit it
+// (chunk j, j + 1, ...).
+//
+// Both kernels: 256 threads, one CTA per SM (192 KB shared memory, 512 TMEM
+// columns):
+//   warps 0-3  compute (thread = TMEM lane = one row of the stationary tile)
+//   warp  4    TMA producer
+//   warp  5    MMA issuer (one thread) and TMEM owner
+//   warp  6    waits on the hand-offs and releases the MMA warp through named
+//              barrier 1 (the issuing thread never waits on an mbarrier)
+//   warp  7    idle
+//
+// dQ kernel, per 128-query tile, TMEM: S [0,128), dP [128,256), dQ [256,384).
+//   S = Q K^T, dP = dO V^T; dS (bf16) overwrites the first 64 columns of S;
+//   dQ += dS K (A from TMEM, B = K MN-major).
+// dK/dV kernel, per 128-key tile, TMEM: S^T [0,128), dP^T [128,256),
+//   dV [256,384), dK [384,512).  S^T = K Q^T, dP^T = V dO^T; P^T and dS^T
+//   (bf16) overwrite the first 64 columns of each; dV += P^T dO, dK += dS^T Q.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "work.cuh"
+
+namespace cpattn {
+
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kT = 128;  // rows of a tile (queries or keys)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kInf = __builtin_huge_valf();
+constexpr int kErrTimeout = 6;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = kT * D * 2;
+  static constexpr int kStages = 2;
+  // Stationary tiles A0, A1 (dQ kernel: Q, dO; dK/dV kernel: K, V) and the
+  // stage rings B0, B1 of the streamed tiles (dQ: K, V; dK/dV: Q, dO).
+  static constexpr int kA0Off = 0;
+  static constexpr int kA1Off = kTileBytes;
+  static constexpr int kB0Off = 2 * kTileBytes;
+  static constexpr int kB1Off = kB0Off + kStages * kTileBytes;
+  // dK/dV kernel: per streamed query tile, LSE * log2 e and D of its 128
+  // queries, two buffers (float [2][2][128]).
+  static constexpr int kVecOff = kB1Off + kStages * kTileBytes;
+  static constexpr int kBarOff = kVecOff + 2 * 2 * kT * 4;
+  // a_full, b0_full[S], b0_empty[S], b1_full[S], b1_empty[S], s_full, p_full,
+  // o_done, drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 4;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// Query chunks visited by a stationary query block: the forward's ring (KV
+// chunk (i - s) mod c at step s), restricted to keys below q_blk_end on the
+// diagonal when causal.
+struct QRing {
+  int L, c, chunk, i, causal, q_blk_end;
+  __device__ __forceinline__ void seg(int s, int& lo, int& n_tiles, int& end) const {
+    n_tiles = 0;
+    lo = 0;
+    end = 0;
+    if (s >= c) return;
+    int j = i - s;
+    if (j < 0) j += c;
+    lo = min(j * chunk, L);
+    end = min((j + 1) * chunk, L);
+    int hi = end;
+    if (causal) {
+      if (j > i) return;
+      if (j == i) hi = min(hi, q_blk_end);
+    }
+    if (hi > lo) n_tiles = (hi - lo + kT - 1) / kT;
+  }
+};
+
+// Query chunks that see a stationary key block of chunk j, in the order they
+// visit it around the ring: chunk (j + s) mod c at step s; causal keeps the
+// chunks at or after j, and on chunk j the query tiles from the key block on.
+struct KRing {
+  int L, c, chunk, j, causal, kv0;
+  __device__ __forceinline__ void seg(int s, int& lo, int& n_tiles, int& end) const {
+    n_tiles = 0;
+    lo = 0;
+    end = 0;
+    if (s >= c) return;
+    int i = j + s;
+    if (i >= c) i -= c;
+    if (causal && i < j) return;
+    lo = min(i * chunk, L);
+    end = min((i + 1) * chunk, L);
+    if (causal && i == j) lo = kv0;
+    if (end > lo) n_tiles = (end - lo + kT - 1) / kT;
+  }
+};
+
+template <class R>
+struct Walk {  // flattened (step, tile) sequence of a ring
+  int s, kt, nt, lo, end;
+  __device__ __forceinline__ void skip_empty(const R& r) {
+    while (s < r.c) {
+      r.seg(s, lo, nt, end);
+      if (nt > 0) return;
+      ++s;
+    }
+  }
+  __device__ __forceinline__ void start(const R& r) {
+    s = 0;
+    kt = 0;
+    skip_empty(r);
+  }
+  __device__ __forceinline__ void advance(const R& r) {
+    if (++kt < nt) return;
+    kt = 0;
+    ++s;
+    skip_empty(r);
+  }
+  __device__ __forceinline__ bool done(const R& r) const { return s >= r.c; }
+  __device__ __forceinline__ int tile_row() const { return lo + kt * kT; }
+};
+
+template <class R>
+__device__ __forceinline__ int count_tiles(const R& r) {
+  Walk<R> w;
+  w.start(r);
+  int n = 0;
+  for (; !w.done(r); w.advance(r)) ++n;
+  return n;
+}
+
+__device__ __forceinline__ void raise_error(WsHeader* hdr, int code) {
+  atomicCAS(&hdr->error, 0, code);
+}
+
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 200000000ull) return false;  // 0.2 s
+  }
+  return true;
+}
+
+// Shared-memory descriptor words (start address >> 4 in the low 14 bits plus
+// the leading byte offset; the high word is constant).
+template <int D>
+struct Desc {
+  uint32_t hi_k, hi_mn;
+  __device__ __forceinline__ Desc() {
+    hi_k = static_cast<uint32_t>(sdesc_sw128(0, 16, 1024) >> 32);
+    hi_mn = static_cast<uint32_t>(sdesc_sw128(0, 16384, 1024) >> 32);
+  }
+  __device__ __forceinline__ uint32_t lo_k(uint32_t addr) const {
+    return static_cast<uint32_t>(sdesc_sw128(addr, 16, 1024));
+  }
+  __device__ __forceinline__ uint32_t lo_mn(uint32_t addr) const {
+    return static_cast<uint32_t>(sdesc_sw128(addr, 16384, 1024));
+  }
+};
+
+// C[128 x 128] (TMEM col d) = A[128 x D] B[128 x D]^T, both K-major in
+// shared memory (descriptor low words a, b).
+template <int D>
+__device__ __forceinline__ void mma_abt(uint32_t d, uint32_t a, uint32_t b, uint32_t hi) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, kT, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+    mma_ss(d, pack_u64(a + off, hi), pack_u64(b + off, hi), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// C[128 x D] (TMEM col d) (+)= A[128 x 128] (TMEM col a, bf16 pairs) * B[128 x D]
+// with B MN-major in shared memory (descriptor low word b).
+template <int D>
+__device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b, uint32_t hi,
+                                           bool acc) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    mma_ts(d, a + kk * 8, pack_u64(b + ((kk * 2048) >> 4), hi), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+}
+
+// Loads a 128-row bf16 tile (rows row0.., head h) into shared memory.
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int h, int row0, uint64_t pol) {
+#pragma unroll
+  for (int hf = 0; hf < D / 64; ++hf)
+    tma_load_3d(dst + hf * 16384, map, bar, hf * 64, h, row0, pol);
+}
+
+// One thread's row of a [128 x D] fp32 TMEM accumulator, times `mul`, to bf16
+// in global memory (16-byte stores).
+template <int D>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, __nv_bfloat16* dst,
+                                          bool valid) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    uint32_t r[32];
+    tmem_ld32(taddr + q * 32, r);
+    tmem_wait_ld();
+    reg_fence32(r);
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        d4[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+  }
+}
+
+struct UnitIds {
+  int tok0, L, h, c, rank, blk, chunk;
+};
+
+__device__ __forceinline__ UnitIds decode(const CtaWork& w) {
+  UnitIds u;
+  u.tok0 = w.x;
+  u.L = w.y;
+  u.h = static_cast<int>(static_cast<unsigned>(w.z) >> 8);
+  u.c = w.z & 0xff;
+  u.rank = w.w & 0xff;
+  u.blk = static_cast<int>(static_cast<unsigned>(w.w) >> 8);
+  u.chunk = cdiv(u.L, u.c);
+  return u;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ delta --
+// Two rows per warp: 16 lanes x 8 features (16-byte loads) per row at D=128.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta,
+                                                        long long rows) {
+  constexpr int kLanesPerRow = D / 8;                // 16 at D=128, 8 at D=64
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r0 = warp_id * kRowsPerWarp; r0 < rows; r0 += n_warps * kRowsPerWarp) {
+    const long long r = r0 + lane / kLanesPerRow;
+    float acc = 0.f;
+    if (r < rows) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + r * D) + lane % kLanesPerRow);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + r * D) + lane % kLanesPerRow);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]);
+        const float2 y = __bfloat1622float2(b2[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+#pragma unroll
+    for (int o = kLanesPerRow / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (r < rows && lane % kLanesPerRow == 0) delta[r] = acc;
+  }
+}
+
+// -------------------------------------------------------------- dK / dV --
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  const int x_cta = static_cast<int>(blockIdx.x);
+  const int n_ctas = __ldcg(&p.hdr->n_items);
+  const int err0 = __ldcg(&p.hdr->error);
+  const CtaWork work = __ldg(&p.table[x_cta]);
+  if (x_cta >= n_ctas) return;
+  if (err0 == kErrTimeout) return;
+
+  const UnitIds u = decode(work);
+  const int kv0 = min(u.rank * u.chunk, u.L) + u.blk * kT;        // first key of the tile
+  const int kv_blk_end = min(kv0 + kT, min((u.rank + 1) * u.chunk, u.L));
+  KRing ring{u.L, u.c, u.chunk, u.rank, p.causal, kv0};
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* a_full = bars;
+  uint64_t* b0_full = bars + 1;
+  uint64_t* b0_empty = b0_full + C::kStages;
+  uint64_t* b1_full = b0_empty + C::kStages;
+  uint64_t* b1_empty = b1_full + C::kStages;
+  uint64_t* s_full = b1_empty + C::kStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [buf][lse2 | delta][128]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 4 && lane == 0) {
+    mbar_init(a_full, 1);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(&b0_full[st], 1);
+      mbar_init(&b0_empty[st], 1);
+      mbar_init(&b1_full[st], 1);
+      mbar_init(&b1_empty[st], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kT);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    const uint64_t pol_kv = l2_policy_evict_first();
+    const uint64_t pol_q = l2_policy_evict_last();
+    mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
+    load_tile<D>(smem + C::kA0Off, &tm_k, a_full, u.h, u.tok0 + kv0, pol_kv);
+    load_tile<D>(smem + C::kA1Off, &tm_v, a_full, u.h, u.tok0 + kv0, pol_kv);
+    Walk<KRing> w;
+    w.start(ring);
+    if (!w.done(ring)) {  // query tile 0 goes to stage 0, which is free
+      const int row = u.tok0 + w.tile_row();
+      mbar_arrive_expect_tx(&b0_full[0], C::kTileBytes);
+      load_tile<D>(smem + C::kB0Off, &tm_q, &b0_full[0], u.h, row, pol_q);
+      mbar_arrive_expect_tx(&b1_full[0], C::kTileBytes);
+      load_tile<D>(smem + C::kB1Off, &tm_do, &b1_full[0], u.h, row, pol_q);
+    }
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 4) {
+    // -------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_last();
+      Walk<KRing> w;
+      w.start(ring);
+      int nb0 = 0, nb1 = 0;
+      if (!w.done(ring)) {
+        nb0 = nb1 = 1;
+        w.advance(ring);
+      }
+      bool ok = true;
+      for (; !w.done(ring); w.advance(ring)) {
+        const int x = nb0;
+        const int st = x % C::kStages;
+        const uint32_t ph = (x / C::kStages) & 1;
+        const int row = u.tok0 + w.tile_row();
+        ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
+        load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_q, &b0_full[st], u.h, row, pol_q);
+        ++nb0;
+        ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
+        load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_do, &b1_full[st], u.h, row, pol_q);
+        ++nb1;
+      }
+      if (!ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
+      wait_drain(a_full, 0);
+      for (int st = 0; st < C::kStages; ++st) {
+        if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
+        if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer --
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Desc<D> dsc;
+    const uint32_t k_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
+    const uint32_t v_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
+    const uint32_t q_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
+    const uint32_t do_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
+    const uint32_t q_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
+    const uint32_t do_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB1Off));
+    constexpr uint32_t kStageLo = C::kTileBytes >> 4;
+    const int n = count_tiles(ring);
+    named_bar_sync(1, 64);  // K, V and query tile 0 landed
+    if (lane == 0 && n > 0) {
+      tc_fence_after();
+      mma_abt<D>(tmem, k_lo, q_lo_k, dsc.hi_k);            // S^T = K Q^T
+      mma_abt<D>(tmem + kT, v_lo, do_lo_k, dsc.hi_k);      // dP^T = V dO^T
+      mma_commit(s_full);
+    }
+    __syncwarp();
+    for (int x = 0; x < n; ++x) {
+      const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
+      const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+      named_bar_sync(1, 64);  // P^T, dS^T in TMEM; next query tile landed
+      if (lane == 0) {
+        tc_fence_after();
+        mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
+        mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
+        mma_commit(&b0_empty[st]);
+        mma_commit(&b1_empty[st]);
+        if (x == n - 1) mma_commit(o_done);
+        if (x + 1 < n) {
+          mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_abt<D>(tmem + kT, v_lo, do_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_commit(s_full);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      mma_commit(drain);
+      wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // --------------------------------------------- waits for the MMA warp --
+    const int n = count_tiles(ring);
+    bool ok = true;
+    if (lane == 0) {
+      ok = wait_bounded(a_full, 0, abort_flag);
+      if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
+      if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
+    }
+    __syncwarp();
+    named_bar_sync(1, 64);
+    for (int x = 0; x < n; ++x) {
+      if (lane == 0 && ok) {
+        ok = wait_bounded(p_full, x & 1, abort_flag);
+        if (ok && x + 1 < n) {
+          const int st1 = (x + 1) % C::kStages;
+          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+          ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+          if (ok) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        }
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);
+    }
+    if (lane == 0 && !ok) {
+      raise_error(p.hdr, kErrTimeout);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // -------------------------------------------------------------- compute --
+    // Thread r owns key kv0 + r (TMEM lane r).  For each streamed query tile:
+    // P^T[r, i] = 2^(S^T[r, i] * scale log2 e - LSE_i log2 e) over the queries
+    // i that see key r, dS^T[r, i] = P^T[r, i] (dP^T[r, i] - D_i).
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const int r = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t row_addr = tmem + lane_base;
+    const int k_pos = kv0 + r;
+    const bool key_valid = k_pos < kv_blk_end;
+    const float c2 = p.scale_log2;
+    const int n = count_tiles(ring);
+    bool ok = true;
+    Walk<KRing> w;
+    w.start(ring);
+    for (int x = 0; x < n; ++x, w.advance(ring)) {
+      const int qt0 = w.tile_row();  // first query of the tile (sample position)
+      float* lse_s = vec + (x & 1) * 2 * kT;
+      float* dlt_s = lse_s + kT;
+      {
+        // Column r of this tile: query qt0 + r, if it belongs to the chunk.
+        const int qp = qt0 + r;
+        float l2 = kInf, dl = 0.f;  // +inf: P = 0 for columns outside the chunk
+        if (qp < w.end) {
+          const size_t ri = static_cast<size_t>(u.tok0 + qp) * p.num_heads + u.h;
+          l2 = __ldg(&p.lse[ri]) * kLog2e;
+          dl = __ldg(&p.delta[ri]);
+        }
+        lse_s[r] = l2;
+        dlt_s[r] = dl;
+      }
+      named_bar_sync(2, kT);  // the column statistics are in shared memory
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        // Causal: query i sees key k_pos iff qt0 + i >= k_pos.
+        const int col_lo = p.causal ? max(0, k_pos - qt0) : 0;
+#pragma unroll
+        for (int q = 0; q < kT / 32; ++q) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(row_addr + q * 32, sv);
+          tmem_ld32(row_addr + kT + q * 32, dv);
+          tmem_wait_ld();
+          reg_fence32(sv);
+          reg_fence32(dv);
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = q * 32 + 2 * e;
+            float p0 = ex2_approx(__uint_as_float(sv[2 * e]) * c2 - lse_s[c0]);
+            float p1 = ex2_approx(__uint_as_float(sv[2 * e + 1]) * c2 - lse_s[c0 + 1]);
+            if (c0 < col_lo) p0 = 0.f;
+            if (c0 + 1 < col_lo) p1 = 0.f;
+            const float d0 = p0 * (__uint_as_float(dv[2 * e]) - dlt_s[c0]);
+            const float d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - dlt_s[c0 + 1]);
+            pw[e] = pack_bf16x2(p0, p1);
+            dw[e] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(row_addr + q * 16, pw);
+          tmem_st16(row_addr + kT + q * 16, dw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        const size_t ri = static_cast<size_t>(u.tok0 + k_pos) * p.num_heads + u.h;
+        store_row<D>(row_addr + 2 * kT, 1.f, p.dv + ri * D, key_valid);
+        store_row<D>(row_addr + 3 * kT, p.scale, p.dk + ri * D, key_valid);
+        tc_fence_before();
+      }
+    }
+    if (!ok) {
+      raise_error(p.hdr, kErrTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------- dQ --
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  const int x_cta = static_cast<int>(blockIdx.x);
+  const int n_ctas = __ldcg(&p.hdr->n_items);
+  const int err0 = __ldcg(&p.hdr->error);
+  const CtaWork work = __ldg(&p.table[x_cta]);
+  if (x_cta >= n_ctas) return;
+  if (err0 == kErrTimeout) return;
+
+  const UnitIds u = decode(work);
+  const int q0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
+  const int q_blk_end = min(q0 + kT, min((u.rank + 1) * u.chunk, u.L));
+  QRing ring{u.L, u.c, u.chunk, u.rank, p.causal, q_blk_end};
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* a_full = bars;
+  uint64_t* b0_full = bars + 1;
+  uint64_t* b0_empty = b0_full + C::kStages;
+  uint64_t* b1_full = b0_empty + C::kStages;
+  uint64_t* b1_empty = b1_full + C::kStages;
+  uint64_t* s_full = b1_empty + C::kStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 4 && lane == 0) {
+    mbar_init(a_full, 1);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(&b0_full[st], 1);
+      mbar_init(&b0_empty[st], 1);
+      mbar_init(&b1_full[st], 1);
+      mbar_init(&b1_empty[st], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kT);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
+    load_tile<D>(smem + C::kA0Off, &tm_q, a_full, u.h, u.tok0 + q0, pol_q);
+    load_tile<D>(smem + C::kA1Off, &tm_do, a_full, u.h, u.tok0 + q0, pol_q);
+    Walk<QRing> w;
+    w.start(ring);
+    if (!w.done(ring)) {
+      const int row = u.tok0 + w.tile_row();
+      mbar_arrive_expect_tx(&b0_full[0], C::kTileBytes);
+      load_tile<D>(smem + C::kB0Off, &tm_k, &b0_full[0], u.h, row, pol_kv);
+      mbar_arrive_expect_tx(&b1_full[0], C::kTileBytes);
+      load_tile<D>(smem + C::kB1Off, &tm_v, &b1_full[0], u.h, row, pol_kv);
+    }
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 4) {
+    // -------------------------------------------------------- TMA producer --
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      Walk<QRing> w;
+      w.start(ring);
+      int nb0 = 0, nb1 = 0;
+      if (!w.done(ring)) {
+        nb0 = nb1 = 1;
+        w.advance(ring);
+      }
+      bool ok = true;
+      for (; !w.done(ring); w.advance(ring)) {
+        const int x = nb0;
+        const int st = x % C::kStages;
+        const uint32_t ph = (x / C::kStages) & 1;
+        const int row = u.tok0 + w.tile_row();
+        ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
+        load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_k, &b0_full[st], u.h, row, pol_kv);
+        ++nb0;
+        ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
+        load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_v, &b1_full[st], u.h, row, pol_kv);
+        ++nb1;
+      }
+      if (!ok) {
+        raise_error(p.hdr, kErrTimeout);
+        *abort_flag = 1;
+      }
+      wait_drain(a_full, 0);
+      for (int st = 0; st < C::kStages; ++st) {
+        if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
+        if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer --
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Desc<D> dsc;
+    const uint32_t q_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
+    const uint32_t do_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
+    const uint32_t k_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
+    const uint32_t v_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
+    const uint32_t k_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
+    constexpr uint32_t kStageLo = C::kTileBytes >> 4;
+    const int n = count_tiles(ring);
+    named_bar_sync(1, 64);  // Q, dO and KV tile 0 landed
+    if (lane == 0 && n > 0) {
+      tc_fence_after();
+      mma_abt<D>(tmem, q_lo, k_lo_k, dsc.hi_k);          // S = Q K^T
+      mma_abt<D>(tmem + kT, do_lo, v_lo_k, dsc.hi_k);    // dP = dO V^T
+      mma_commit(s_full);
+      mma_commit(&b1_empty[0]);                          // V consumed
+    }
+    __syncwarp();
+    for (int x = 0; x < n; ++x) {
+      const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
+      const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+      named_bar_sync(1, 64);  // dS in TMEM; next KV tile landed
+      if (lane == 0) {
+        tc_fence_after();
+        mma_tmem_a<D>(tmem + 2 * kT, tmem, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
+        mma_commit(&b0_empty[st]);                                                       // K consumed
+        if (x == n - 1) mma_commit(o_done);
+        if (x + 1 < n) {
+          mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_abt<D>(tmem + kT, do_lo, v_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_commit(s_full);
+          mma_commit(&b1_empty[st1]);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      mma_commit(drain);
+      wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // --------------------------------------------- waits for the MMA warp --
+    const int n = count_tiles(ring);
+    bool ok = true;
+    if (lane == 0) {
+      ok = wait_bounded(a_full, 0, abort_flag);
+      if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
+      if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
+    }
+    __syncwarp();
+    named_bar_sync(1, 64);
+    for (int x = 0; x < n; ++x) {
+      if (lane == 0 && ok) {
+        ok = wait_bounded(p_full, x & 1, abort_flag);
+        if (ok && x + 1 < n) {
+          const int st1 = (x + 1) % C::kStages;
+          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+          ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+          if (ok) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        }
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);
+    }
+    if (lane == 0 && !ok) {
+      raise_error(p.hdr, kErrTimeout);
+      *abort_flag = 1;
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // -------------------------------------------------------------- compute --
+    // Thread r owns query q0 + r.  For each KV tile: P = 2^(S * scale log2 e -
+    // LSE log2 e) over the visible keys (a prefix of the tile), dS = P (dP - D).
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const int r = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t row_addr = tmem + lane_base;
+    const int q_pos = q0 + r;
+    const bool row_valid = q_pos < q_blk_end;
+    const size_t ri = static_cast<size_t>(u.tok0 + q_pos) * p.num_heads + u.h;
+    const float lse2 = row_valid ? __ldg(&p.lse[ri]) * kLog2e : 0.f;
+    const float dlt = row_valid ? __ldg(&p.delta[ri]) : 0.f;
+    const float c2 = p.scale_log2;
+    const int n = count_tiles(ring);
+    bool ok = true;
+    Walk<QRing> w;
+    w.start(ring);
+    for (int x = 0; x < n && ok; ++x, w.advance(ring)) {
+      ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int kv0 = w.tile_row();
+      const int lim = p.causal ? min(w.end, q_pos + 1) : w.end;
+      const int nvis = lim - kv0;  // visible keys: a prefix of the tile
+#pragma unroll
+      for (int q = 0; q < kT / 32; ++q) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(row_addr + q * 32, sv);
+        tmem_ld32(row_addr + kT + q * 32, dv);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(dv);
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = q * 32 + 2 * e;
+          float p0 = ex2_approx(__uint_as_float(sv[2 * e]) * c2 - lse2);
+          float p1 = ex2_approx(__uint_as_float(sv[2 * e + 1]) * c2 - lse2);
+          if (c0 >= nvis) p0 = 0.f;
+          if (c0 + 1 >= nvis) p1 = 0.f;
+          dw[e] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * e]) - dlt),
+                              p1 * (__uint_as_float(dv[2 * e + 1]) - dlt));
+        }
+        tmem_st16(row_addr + q * 16, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        store_row<D>(row_addr + 2 * kT, p.scale, p.dq + ri * D, row_valid);
+        tc_fence_before();
+      }
+    }
+    if (!ok) {
+      raise_error(p.hdr, kErrTimeout);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), C::kTmemCols);
+  }
+}
+
+int bwd_smem_bytes(int D) {
+  return D == 64 ? BwdCfg<64>::kSmemBytes : BwdCfg<128>::kSmemBytes;
+}
+
+cudaError_t launch_bwd_delta(const __nv_bfloat16* out, const __nv_bfloat16* dout,
+                             float* delta, long long rows, int D, int num_sms,
+                             cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const long long warps_needed = (rows + 1) / 2;
+  long long blocks = (warps_needed + 7) / 8;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (D == 64)
+    bwd_delta_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, dout, delta, rows);
+  else
+    bwd_delta_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, dout, delta, rows);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                                              BwdParams),
+                                 const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo,
+                                 const BwdParams& p, long long grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BwdCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(
+      tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const BwdParams& p, int D, long long grid, cudaStream_t stream) {
+  if (D == 64) return launch_kernel<64>(attn_bwd_dkdv_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
+  return launch_kernel<128>(attn_bwd_dkdv_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const BwdParams& p, int D, long long grid, cudaStream_t stream) {
+  if (D == 64) return launch_kernel<64>(attn_bwd_dq_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
+  return launch_kernel<128>(attn_bwd_dq_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
+}
+
+}  // namespace cpattn

@@ -64,7 +64,11 @@ struct SchedParams {
   int* first_cta;      // [B + 1]: first CTA of the sample at each order position
   int* order;          // [B]: samples by decreasing length
   CtaWork* table;      // [max_ctas]: work of each CTA (first n_items used)
+  // Optional second table over the same items in the opposite order within
+  // each (sample, head): increasing item index (null: not written).
+  CtaWork* table_asc;
   long long max_ctas;  // grid size the host launches
+  int rows_per_item;   // query (or key) rows per item
 };
 
 struct FwdParams {
@@ -79,6 +83,22 @@ struct FwdParams {
   float* m_steps;       // partials: [S, T, H]
   float* l_steps;
   long long total_tokens;
+  WsHeader* hdr;
+};
+
+// Backward kernels (attn_bwd.cu).  Gradients are bf16 [T, H, D]; `lse` is
+// the forward's natural-log LSE [T, H]; `delta` = rowsum(dO * O) [T, H].
+struct BwdParams {
+  const CtaWork* table;  // this kernel's work table (written by the schedule kernel)
+  const float* lse;
+  const float* delta;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int num_heads;
+  int causal;
+  float scale;       // softmax scale (applied to dQ and dK at the end)
+  float scale_log2;  // softmax scale * log2(e)
   WsHeader* hdr;
 };
 
@@ -128,6 +148,22 @@ int attn_smem_bytes(int D);
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const FwdParams& p, int D,
                         bool partials, long long grid, cudaStream_t stream);
+
+int bwd_smem_bytes(int D);
+
+// delta[r] = sum_d dO[r, d] * O[r, d] for rows r < rows (= T * H).
+cudaError_t launch_bwd_delta(const __nv_bfloat16* out, const __nv_bfloat16* dout,
+                             float* delta, long long rows, int D, int num_sms,
+                             cudaStream_t stream);
+
+// dK/dV kernel (one CTA per 128-key tile) and dQ kernel (one CTA per 128-query
+// tile); the four tensor maps are Q, K, V, dO.
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const BwdParams& p, int D, long long grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const BwdParams& p, int D, long long grid, cudaStream_t stream);
 
 cudaError_t launch_merge(const MergeParams& p, int D, bool bf16_out,
                          int num_sms, cudaStream_t stream);

@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(kSchedThreads)
     long long cnt = 0;
     if (k < p.num_seqs)
       cnt = static_cast<long long>(
-                sample_items(sample_geom(p.cu_seqlens, p.cp_size, p.order[k]))) *
+                sample_items(sample_geom(p.cu_seqlens, p.cp_size, p.order[k]),
+                             p.rows_per_item)) *
             p.num_heads;
     const long long incl = block_scan(cnt, warp_sums);
     if (k < p.num_seqs) p.first_cta[k] = static_cast<int>(s_carry + incl - cnt);
@@ -144,8 +145,9 @@ __global__ void __launch_bounds__(kSchedThreads)
     }
     int next = p.first_cta[pos + 1];
     int b = p.order[pos];
+    const int rows = p.rows_per_item;
     SampleGeom g = sample_geom(p.cu_seqlens, p.cp_size, b);
-    int n_b = sample_items(g);
+    int n_b = sample_items(g, rows);
     int first = p.first_cta[pos];
     for (int x = x_begin; x < x_end; ++x) {
       while (x >= next) {  // samples without CTAs (L = 0) are passed over
@@ -154,15 +156,23 @@ __global__ void __launch_bounds__(kSchedThreads)
         next = p.first_cta[pos + 1];
         b = p.order[pos];
         g = sample_geom(p.cu_seqlens, p.cp_size, b);
-        n_b = sample_items(g);
+        n_b = sample_items(g, rows);
       }
       const int e = x - first;
       const int h = e / n_b;
+      const int local = e - h * n_b;
       int rank, blk;
-      item_coords(g, n_b - 1 - (e - h * n_b), rank, blk);
-      p.table[x] = make_int4(p.cu_seqlens[b], g.L, (h << 8) | g.c,
+      item_coords(g, n_b - 1 - local, rank, blk, rows);
+      const int tok0 = p.cu_seqlens[b];
+      p.table[x] = make_int4(tok0, g.L, (h << 8) | g.c,
                              static_cast<int>((static_cast<unsigned>(blk) << 8) |
                                               static_cast<unsigned>(rank)));
+      if (p.table_asc != nullptr) {
+        item_coords(g, local, rank, blk, rows);
+        p.table_asc[x] = make_int4(tok0, g.L, (h << 8) | g.c,
+                                   static_cast<int>((static_cast<unsigned>(blk) << 8) |
+                                                    static_cast<unsigned>(rank)));
+      }
     }
   }
   if (tid == 0) p.hdr->n_items = n_ctas;

@@ -32,18 +32,18 @@ __device__ __forceinline__ SampleGeom sample_geom(const int* cu, const int* cp,
   return g;
 }
 
-// Work items of one sample (its blocks over all ranks).
-__device__ __forceinline__ int sample_items(const SampleGeom& g) {
+// Work items of one sample (its blocks of `rows` rows over all ranks).
+__device__ __forceinline__ int sample_items(const SampleGeom& g, int rows = kRowsPerItem) {
   if (g.L == 0) return 0;
-  return g.full * cdiv(g.chunk, kRowsPerItem) +
-         (g.rem > 0 ? cdiv(g.rem, kRowsPerItem) : 0);
+  return g.full * cdiv(g.chunk, rows) + (g.rem > 0 ? cdiv(g.rem, rows) : 0);
 }
 
 // Item `local` of a sample -> (rank, block).  For causal attention the cost
-// (KV tiles visited) never decreases with `local`.
+// of a query block (KV tiles visited) never decreases with `local`; the cost
+// of a key block (query tiles that see it) never increases with it.
 __device__ __forceinline__ void item_coords(const SampleGeom& g, int local,
-                                            int& rank, int& blk) {
-  const int per = cdiv(g.chunk, kRowsPerItem);
+                                            int& rank, int& blk, int rows = kRowsPerItem) {
+  const int per = cdiv(g.chunk, rows);
   rank = local / per;
   blk = local - rank * per;
   if (rank >= g.full) {  // the short last chunk

@@ -26,6 +26,40 @@ def check_attention(out, lse, ref_o, ref_lse, what=""):
     return do, dl
 
 
+# Gradients (bf16 outputs of cpattn_bwd) against the float64 oracle.  Rounding
+# points of the GPU path: P and dS are rounded to bf16 (relative 2^-9) before
+# their products, O (bf16) enters D = rowsum(dO * O), and each gradient is
+# rounded to bf16 (relative 2^-9).  A rounding error of relative size 2^-9 on
+# each of the N terms of a gradient sum adds up like a random walk to about
+# 2^-9 * sqrt(sum of squared terms) -- a fraction of a percent of the RMS of
+# the gradient -- so:
+#   * RMS(error) <= GRAD_RMS_RTOL * RMS(gradient) over each tensor (a dropped
+#     or wrongly scaled term gives errors of the order of the gradient itself);
+#   * every element: |error| <= GRAD_RTOL * |g| + GRAD_ATOL_RMS * RMS(gradient)
+#     (the first term bounds the output rounding with 8x margin, the second the
+#     tail of the summed rounding errors over ~1e5-1e6 elements; a wrong mask
+#     on a row gives errors of the order of RMS(gradient) there).
+GRAD_RMS_RTOL = 1e-2
+GRAD_RTOL = 2 ** -6
+GRAD_ATOL_RMS = 0.15
+
+
+def check_grad(got, ref, what=""):
+    """Assert the gradient tolerances; returns (RMS err / RMS ref, worst ratio)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "%s: non-finite gradient" % what
+    if ref.size == 0:
+        return 0.0, 0.0
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    rel_rms = float(np.sqrt(np.mean(err ** 2))) / max(rms, 1e-30)
+    worst = float(np.max(err / (GRAD_RTOL * np.abs(ref) + GRAD_ATOL_RMS * rms + 1e-30)))
+    assert rel_rms <= GRAD_RMS_RTOL, "%s: RMS error / RMS = %g" % (what, rel_rms)
+    assert worst <= 1.0, "%s: worst elementwise error ratio %g" % (what, worst)
+    return rel_rms, worst
+
+
 def make_batch(lengths, H, D, seed, std=1.0, device="cuda"):
     """Seeded THD batch: CPU bf16 q/k/v, int32 cu_seqlens, and GPU copies."""
     T = int(sum(lengths))
