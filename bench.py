@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=[None, "main", "long128k", "merge8"],
+    ap.add_argument("--only", default=None,
+                    choices=[None, "main", "long128k", "merge8", "backward"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -296,8 +297,9 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8"):
-        fn = run_long128k if args.only == "long128k" else run_merge8
+    if args.only in ("long128k", "merge8", "backward"):
+        fn = {"long128k": run_long128k, "merge8": run_merge8,
+              "backward": run_backward}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -426,7 +428,7 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for fn in (run_long128k, run_merge8):
+        for fn in (run_long128k, run_merge8, run_backward):
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
     clk = clocks.stop()
@@ -519,6 +521,50 @@ def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     del q, k, v, out, lse
     torch.cuda.empty_cache()
     return res
+
+
+def run_backward(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                 bf16_sustained, hbm_peak):
+    """cpattn_bwd (dQ, dK, dV) after a forward, on the packed 16K batch and on
+    the 131,072-token sequence.  FLOPs: 2.5 x the forward's (five matmuls over
+    the visible pairs: S recomputed, dP, dV, dK, dQ)."""
+    import numpy as np
+    sub = {}
+    for name in ("packed16k", "long128k"):
+        w = workloads.WORKLOADS[name]
+        H, D = w["H"], w["D"]
+        if name == "packed16k":
+            lengths = workloads.packed_lengths(args.seed, w["budget"])
+            plan = cpattn.plan(lengths, w["world"], w["limit"], w["max_cp"])
+            cps_l = [int(x) for x in plan["cp_size"]]
+            std, steps = 1.0, max(3, min(args.steps, 20))
+        else:
+            lengths, cps_l, std = list(w["lengths"]), [w["cp"]], w["std"]
+            steps = max(3, min(args.steps, 5))
+        T, max_cp = sum(lengths), max(cps_l)
+        q, k, v = workloads.qkv_device(T, H, D, args.seed, std=std, device=dev)
+        g = torch.Generator(device=dev).manual_seed(args.seed + 1)
+        dout = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+        cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+        cps = torch.tensor(cps_l, dtype=torch.int32, device=dev)
+        out, lse = cpattn.fwd(q, k, v, cu, cps, max_seqlen=max(lengths), max_cp=max_cp)
+        ws = cpattn.alloc_bwd_workspace(T, len(lengths), H, D, max_cp, dev)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        fn = lambda: cpattn.bwd(q, k, v, out, dout, lse, cu, cps,  # noqa: E731
+                                max_seqlen=max(lengths), max_cp=max_cp, dq=dq, dk=dk, dv=dv,
+                                workspace=ws)
+        clocks.mark(True)
+        ms = time_loop(torch, fn, steps, 2, stream)
+        clocks.mark(False)
+        assert cpattn.poll_error(ws) == cpattn.OK
+        flops = 2.5 * attention_flops(lengths, H, D)
+        tf = flops / (ms * 1e-3) / 1e12
+        sub[name] = {"ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+                     "frac_of_sustained": tf / bf16_sustained, "flops": flops, "steps": steps}
+        del q, k, v, dout, out, lse, ws, dq, dk, dv
+        torch.cuda.empty_cache()
+    return {"backward": {"what": "cpattn_bwd (delta + dK/dV + dQ kernels), inputs resident; "
+                                 "FLOPs = 2.5 x forward (5 matmuls over visible pairs)", **sub}}
 
 
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,

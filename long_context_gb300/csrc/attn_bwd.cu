@@ -14,21 +14,25 @@
 // walks the query chunks that see its key block in the order they visit it
 // (chunk j, j + 1, ...).
 //
-// Both kernels: 256 threads, one CTA per SM (192 KB shared memory, 512 TMEM
+// Both kernels: 384 threads, one CTA per SM (192 KB shared memory, 512 TMEM
 // columns):
-//   warps 0-3  compute (thread = TMEM lane = one row of the stationary tile)
-//   warp  4    TMA producer
-//   warp  5    MMA issuer (one thread) and TMEM owner
-//   warp  6    waits on the hand-offs and releases the MMA warp through named
+//   warps 0-7  compute: warps w and w + 4 share the TMEM lanes of quarter w
+//              (thread = one row of the stationary tile), for the first and
+//              the second 64 columns of each streamed tile
+//   warp  8    TMA producer
+//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warp  10   waits on the hand-offs and releases the MMA warp through named
 //              barrier 1 (the issuing thread never waits on an mbarrier)
-//   warp  7    idle
+//   warp  11   idle
 //
 // dQ kernel, per 128-query tile, TMEM: S [0,128), dP [128,256), dQ [256,384).
-//   S = Q K^T, dP = dO V^T; dS (bf16) overwrites the first 64 columns of S;
-//   dQ += dS K (A from TMEM, B = K MN-major).
+//   S = Q K^T, dP = dO V^T; dS (bf16 pairs) of key columns [0,64) and
+//   [64,128) overwrites dP columns [0,32) and [64,96); dQ += dS K (A from
+//   TMEM, B = K MN-major).
 // dK/dV kernel, per 128-key tile, TMEM: S^T [0,128), dP^T [128,256),
 //   dV [256,384), dK [384,512).  S^T = K Q^T, dP^T = V dO^T; P^T and dS^T
-//   (bf16) overwrite the first 64 columns of each; dV += P^T dO, dK += dS^T Q.
+//   (bf16 pairs) overwrite columns [0,32) and [64,96) of their regions;
+//   dV += P^T dO, dK += dS^T Q.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -39,7 +43,8 @@ namespace cpattn {
 
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
+constexpr int kComputeThreads = 256;  // warps 0-7
 constexpr int kT = 128;  // rows of a tile (queries or keys)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInf = __builtin_huge_valf();
@@ -60,8 +65,8 @@ struct BwdCfg {
   static constexpr int kVecOff = kB1Off + kStages * kTileBytes;
   static constexpr int kBarOff = kVecOff + 2 * 2 * kT * 4;
   // a_full, b0_full[S], b0_empty[S], b1_full[S], b1_empty[S], s_full, p_full,
-  // o_done, drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 4;
+  // o_done, drain, dp_full, ds_full
+  static constexpr int kNumBars = 1 + 4 * kStages + 6;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
   static constexpr uint32_t kTmemCols = 512;
@@ -185,15 +190,17 @@ __device__ __forceinline__ void mma_abt(uint32_t d, uint32_t a, uint32_t b, uint
   }
 }
 
-// C[128 x D] (TMEM col d) (+)= A[128 x 128] (TMEM col a, bf16 pairs) * B[128 x D]
-// with B MN-major in shared memory (descriptor low word b).
+// C[128 x D] (TMEM col d) (+)= A[128 x 128] * B[128 x D], B MN-major in
+// shared memory (descriptor low word b).  A is in TMEM as bf16 pairs: its
+// first 64 K-columns packed in columns [a, a + 32), the last 64 in
+// [a + 64, a + 96) (each half written by the warps that own those columns).
 template <int D>
 __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b, uint32_t hi,
                                            bool acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
 #pragma unroll
   for (int kk = 0; kk < kT / 16; ++kk)
-    mma_ts(d, a + kk * 8, pack_u64(b + ((kk * 2048) >> 4), hi), idesc,
+    mma_ts(d, a + kk * 8 + (kk >= 4 ? 32 : 0), pack_u64(b + ((kk * 2048) >> 4), hi), idesc,
            (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -315,6 +322,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* p_full = s_full + 1;
   uint64_t* o_done = p_full + 1;
   uint64_t* drain = o_done + 1;
+  uint64_t* dp_full = drain + 1;  // dP^T ready (S^T ready is s_full)
+  uint64_t* ds_full = dp_full + 1;  // dS^T in TMEM (P^T in TMEM is p_full)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
   float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [buf][lse2 | delta][128]
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     mbar_init(a_full, 1);
     for (int st = 0; st < C::kStages; ++st) {
       mbar_init(&b0_full[st], 1);
@@ -331,9 +340,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&b1_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kT);
+    mbar_init(p_full, kComputeThreads);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, kComputeThreads);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile<D>(smem + C::kB1Off, &tm_do, &b1_full[0], u.h, row, pol_q);
     }
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -363,7 +374,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 4) {
+  if (warp == 8) {
     // -------------------------------------------------------- TMA producer --
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_last();
@@ -401,7 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer --
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Desc<D> dsc;
@@ -413,29 +424,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t do_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB1Off));
     constexpr uint32_t kStageLo = C::kTileBytes >> 4;
     const int n = count_tiles(ring);
+    // Two hand-offs per query tile x: once P^T(x) is in TMEM, dV(x) and then
+    // S^T(x + 1) (which overwrites P^T(x) after dV(x) has read it); once
+    // dS^T(x) is in TMEM, dK(x) and then dP^T(x + 1).  The exponentials of
+    // tile x + 1 thus overlap dK(x) and dP^T(x + 1).
     named_bar_sync(1, 64);  // K, V and query tile 0 landed
     if (lane == 0 && n > 0) {
       tc_fence_after();
       mma_abt<D>(tmem, k_lo, q_lo_k, dsc.hi_k);            // S^T = K Q^T
-      mma_abt<D>(tmem + kT, v_lo, do_lo_k, dsc.hi_k);      // dP^T = V dO^T
       mma_commit(s_full);
+      mma_abt<D>(tmem + kT, v_lo, do_lo_k, dsc.hi_k);      // dP^T = V dO^T
+      mma_commit(dp_full);
     }
     __syncwarp();
     for (int x = 0; x < n; ++x) {
       const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
       const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(1, 64);  // P^T, dS^T in TMEM; next query tile landed
+      named_bar_sync(1, 64);  // P^T(x) in TMEM; query tile x + 1 landed
       if (lane == 0) {
         tc_fence_after();
         mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
+        if (x + 1 < n) {
+          mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_commit(s_full);
+        }
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);  // dS^T(x) in TMEM; dO tile x + 1 landed
+      if (lane == 0) {
+        tc_fence_after();
         mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
         mma_commit(&b0_empty[st]);
         mma_commit(&b1_empty[st]);
         if (x == n - 1) mma_commit(o_done);
         if (x + 1 < n) {
-          mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
           mma_abt<D>(tmem + kT, v_lo, do_lo_k + st1 * kStageLo, dsc.hi_k);
-          mma_commit(s_full);
+          mma_commit(dp_full);
         }
       }
       __syncwarp();
@@ -445,7 +469,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait_drain(drain, 0);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // --------------------------------------------- waits for the MMA warp --
     const int n = count_tiles(ring);
     bool ok = true;
@@ -457,14 +481,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
     named_bar_sync(1, 64);
     for (int x = 0; x < n; ++x) {
+      const int st1 = (x + 1) % C::kStages;
+      const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
       if (lane == 0 && ok) {
         ok = wait_bounded(p_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) {
-          const int st1 = (x + 1) % C::kStages;
-          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-          ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-          if (ok) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-        }
+        if (ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);
+      if (lane == 0 && ok) {
+        ok = wait_bounded(ds_full, x & 1, abort_flag);
+        if (ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
       }
       __syncwarp();
       named_bar_sync(1, 64);
@@ -474,18 +501,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       *abort_flag = 1;
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // -------------------------------------------------------------- compute --
-    // Thread r owns key kv0 + r (TMEM lane r).  For each streamed query tile:
-    // P^T[r, i] = 2^(S^T[r, i] * scale log2 e - LSE_i log2 e) over the queries
-    // i that see key r, dS^T[r, i] = P^T[r, i] (dP^T[r, i] - D_i).
+    // Thread r of warps 0-3 and thread r of warps 4-7 own key kv0 + r (TMEM
+    // lane r), the first for query columns [0, 64), the second for [64, 128).
+    // For each streamed query tile: P^T[r, i] = 2^(S^T[r, i] scale log2 e -
+    // LSE_i log2 e) over the queries i that see key r, and
+    // dS^T[r, i] = P^T[r, i] (dP^T[r, i] - D_i).
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const int r = threadIdx.x;
+    const int r = threadIdx.x & (kT - 1);
+    const int ch = warp >> 2;  // column half
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t row_addr = tmem + lane_base;
     const int k_pos = kv0 + r;
     const bool key_valid = k_pos < kv_blk_end;
     const float c2 = p.scale_log2;
+    const float2 c22 = make_float2(c2, c2);
     const int n = count_tiles(ring);
     bool ok = true;
     Walk<KRing> w;
@@ -495,50 +526,93 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       float* lse_s = vec + (x & 1) * 2 * kT;
       float* dlt_s = lse_s + kT;
       {
-        // Column r of this tile: query qt0 + r, if it belongs to the chunk.
+        // Column r of this tile (query qt0 + r, if it belongs to the chunk):
+        // warps 0-3 load its LSE, warps 4-7 its D.
         const int qp = qt0 + r;
-        float l2 = kInf, dl = 0.f;  // +inf: P = 0 for columns outside the chunk
+        float val = ch == 0 ? kInf : 0.f;  // +inf LSE: P = 0 outside the chunk
         if (qp < w.end) {
           const size_t ri = static_cast<size_t>(u.tok0 + qp) * p.num_heads + u.h;
-          l2 = __ldg(&p.lse[ri]) * kLog2e;
-          dl = __ldg(&p.delta[ri]);
+          val = ch == 0 ? __ldg(&p.lse[ri]) * kLog2e : __ldg(&p.delta[ri]);
         }
-        lse_s[r] = l2;
-        dlt_s[r] = dl;
+        (ch == 0 ? lse_s : dlt_s)[r] = val;
       }
-      named_bar_sync(2, kT);  // the column statistics are in shared memory
+      named_bar_sync(2, kComputeThreads);  // the column statistics are in shared memory
       if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
       if (ok) {
         tc_fence_after();
         // Causal: query i sees key k_pos iff qt0 + i >= k_pos.
         const int col_lo = p.causal ? max(0, k_pos - qt0) : 0;
+        const bool masked = __any_sync(0xffffffffu, col_lo > 64 * ch);
+        const float4* lse4 = reinterpret_cast<const float4*>(lse_s);
+        const float4* dlt4 = reinterpret_cast<const float4*>(dlt_s);
+        // Phase 1: P^T of this half's columns [64 ch, 64 ch + 64), kept in
+        // registers and stored packed to columns [64 ch, 64 ch + 32) of the
+        // S^T region (columns this thread has already read).
+        float pv[64];
 #pragma unroll
-        for (int q = 0; q < kT / 32; ++q) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(row_addr + q * 32, sv);
-          tmem_ld32(row_addr + kT + q * 32, dv);
+        for (int q = 0; q < 2; ++q) {
+          uint32_t sv[32];
+          tmem_ld32(row_addr + ch * 64 + q * 32, sv);
           tmem_wait_ld();
           reg_fence32(sv);
-          reg_fence32(dv);
-          uint32_t pw[16], dw[16];
+          uint32_t pw[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = q * 32 + 2 * e;
-            float p0 = ex2_approx(__uint_as_float(sv[2 * e]) * c2 - lse_s[c0]);
-            float p1 = ex2_approx(__uint_as_float(sv[2 * e + 1]) * c2 - lse_s[c0 + 1]);
-            if (c0 < col_lo) p0 = 0.f;
-            if (c0 + 1 < col_lo) p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(dv[2 * e]) - dlt_s[c0]);
-            const float d1 = p1 * (__uint_as_float(dv[2 * e + 1]) - dlt_s[c0 + 1]);
-            pw[e] = pack_bf16x2(p0, p1);
-            dw[e] = pack_bf16x2(d0, d1);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int c0 = ch * 64 + q * 32 + 4 * e4;
+            const float4 l4 = lse4[c0 / 4];
+#pragma unroll
+            for (int j2 = 0; j2 < 2; ++j2) {
+              const int e = 4 * e4 + 2 * j2;
+              const float2 nl = j2 ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+              const float2 xs = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c22, nl);
+              float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+              if (masked) {
+                if (c0 + 2 * j2 < col_lo) pp.x = 0.f;
+                if (c0 + 2 * j2 + 1 < col_lo) pp.y = 0.f;
+              }
+              pv[q * 32 + e] = pp.x;
+              pv[q * 32 + e + 1] = pp.y;
+              pw[2 * e4 + j2] = pack_bf16x2(pp.x, pp.y);
+            }
           }
-          tmem_st16(row_addr + q * 16, pw);
-          tmem_st16(row_addr + kT + q * 16, dw);
+          tmem_st16(row_addr + ch * 64 + q * 16, pw);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full);
+        // Phase 2: dS^T = P^T (dP^T - D), stored packed over the dP^T region
+        // the same way.
+        ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t dv[32];
+            tmem_ld32(row_addr + kT + ch * 64 + q * 32, dv);
+            tmem_wait_ld();
+            reg_fence32(dv);
+            uint32_t dw[16];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int c0 = ch * 64 + q * 32 + 4 * e4;
+              const float4 d4 = dlt4[c0 / 4];
+#pragma unroll
+              for (int j2 = 0; j2 < 2; ++j2) {
+                const int e = 4 * e4 + 2 * j2;
+                const float2 nd = j2 ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                const float2 ds = __fmul2_rn(
+                    make_float2(pv[q * 32 + e], pv[q * 32 + e + 1]),
+                    __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd));
+                dw[2 * e4 + j2] = pack_bf16x2(ds.x, ds.y);
+              }
+            }
+            tmem_st16(row_addr + kT + ch * 64 + q * 16, dw);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(ds_full);
+        }
       }
     }
     if (ok) {
@@ -546,8 +620,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         const size_t ri = static_cast<size_t>(u.tok0 + k_pos) * p.num_heads + u.h;
-        store_row<D>(row_addr + 2 * kT, 1.f, p.dv + ri * D, key_valid);
-        store_row<D>(row_addr + 3 * kT, p.scale, p.dk + ri * D, key_valid);
+        if (ch == 0)
+          store_row<D>(row_addr + 2 * kT, 1.f, p.dv + ri * D, key_valid);
+        else
+          store_row<D>(row_addr + 3 * kT, p.scale, p.dk + ri * D, key_valid);
         tc_fence_before();
       }
     }
@@ -559,7 +635,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), C::kTmemCols);
   }
@@ -598,13 +674,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* p_full = s_full + 1;
   uint64_t* o_done = p_full + 1;
   uint64_t* drain = o_done + 1;
+  uint64_t* dp_full = drain + 1;   // dP ready (S ready is s_full)
+  uint64_t* ds_full = dp_full + 1;  // dS in TMEM (S read out is p_full)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     mbar_init(a_full, 1);
     for (int st = 0; st < C::kStages; ++st) {
       mbar_init(&b0_full[st], 1);
@@ -613,9 +691,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&b1_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kT);
+    mbar_init(p_full, kComputeThreads);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, kComputeThreads);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
@@ -637,7 +717,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile<D>(smem + C::kB1Off, &tm_v, &b1_full[0], u.h, row, pol_kv);
     }
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -645,7 +725,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 4) {
+  if (warp == 8) {
     // -------------------------------------------------------- TMA producer --
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
@@ -683,7 +763,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer --
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Desc<D> dsc;
@@ -694,28 +774,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t k_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
     constexpr uint32_t kStageLo = C::kTileBytes >> 4;
     const int n = count_tiles(ring);
+    // Two hand-offs per KV tile x: once the compute warps have read S(x),
+    // S(x + 1); once dS(x) is in TMEM (over the dP region), dQ(x) and then
+    // dP(x + 1).  S(x + 1) thus overlaps the dS phase of tile x, and dQ(x),
+    // dP(x + 1) the exponentials of tile x + 1.
     named_bar_sync(1, 64);  // Q, dO and KV tile 0 landed
     if (lane == 0 && n > 0) {
       tc_fence_after();
       mma_abt<D>(tmem, q_lo, k_lo_k, dsc.hi_k);          // S = Q K^T
-      mma_abt<D>(tmem + kT, do_lo, v_lo_k, dsc.hi_k);    // dP = dO V^T
       mma_commit(s_full);
+      mma_abt<D>(tmem + kT, do_lo, v_lo_k, dsc.hi_k);    // dP = dO V^T
+      mma_commit(dp_full);
       mma_commit(&b1_empty[0]);                          // V consumed
     }
     __syncwarp();
     for (int x = 0; x < n; ++x) {
       const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
       const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(1, 64);  // dS in TMEM; next KV tile landed
+      named_bar_sync(1, 64);  // S(x) read out; KV tile x + 1's K landed
+      if (lane == 0 && x + 1 < n) {
+        tc_fence_after();
+        mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
+        mma_commit(s_full);
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);  // dS(x) in TMEM; KV tile x + 1's V landed
       if (lane == 0) {
         tc_fence_after();
-        mma_tmem_a<D>(tmem + 2 * kT, tmem, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
-        mma_commit(&b0_empty[st]);                                                       // K consumed
+        mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
+        mma_commit(&b0_empty[st]);                                                            // K done
         if (x == n - 1) mma_commit(o_done);
         if (x + 1 < n) {
-          mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
           mma_abt<D>(tmem + kT, do_lo, v_lo_k + st1 * kStageLo, dsc.hi_k);
-          mma_commit(s_full);
+          mma_commit(dp_full);
           mma_commit(&b1_empty[st1]);
         }
       }
@@ -726,7 +817,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait_drain(drain, 0);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // --------------------------------------------- waits for the MMA warp --
     const int n = count_tiles(ring);
     bool ok = true;
@@ -738,14 +829,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
     named_bar_sync(1, 64);
     for (int x = 0; x < n; ++x) {
+      const int st1 = (x + 1) % C::kStages;
+      const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
       if (lane == 0 && ok) {
         ok = wait_bounded(p_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) {
-          const int st1 = (x + 1) % C::kStages;
-          const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-          ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-          if (ok) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-        }
+        if (ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+      }
+      __syncwarp();
+      named_bar_sync(1, 64);
+      if (lane == 0 && ok) {
+        ok = wait_bounded(ds_full, x & 1, abort_flag);
+        if (ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
       }
       __syncwarp();
       named_bar_sync(1, 64);
@@ -755,12 +849,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       *abort_flag = 1;
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // -------------------------------------------------------------- compute --
-    // Thread r owns query q0 + r.  For each KV tile: P = 2^(S * scale log2 e -
-    // LSE log2 e) over the visible keys (a prefix of the tile), dS = P (dP - D).
+    // Thread r of warps 0-3 and of warps 4-7 own query q0 + r (TMEM lane r),
+    // for key columns [0, 64) and [64, 128) of each KV tile:
+    // P = 2^(S scale log2 e - LSE log2 e) over the visible keys (a prefix of
+    // the tile) and dS = P (dP - D).
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const int r = threadIdx.x;
+    const int r = threadIdx.x & (kT - 1);
+    const int ch = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t row_addr = tmem + lane_base;
     const int q_pos = q0 + r;
@@ -769,47 +866,97 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float lse2 = row_valid ? __ldg(&p.lse[ri]) * kLog2e : 0.f;
     const float dlt = row_valid ? __ldg(&p.delta[ri]) : 0.f;
     const float c2 = p.scale_log2;
+    const float2 c22 = make_float2(c2, c2);
+    const float2 nl = make_float2(-lse2, -lse2);
+    const float2 nd = make_float2(-dlt, -dlt);
     const int n = count_tiles(ring);
     bool ok = true;
     Walk<QRing> w;
     w.start(ring);
-    for (int x = 0; x < n && ok; ++x, w.advance(ring)) {
-      ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const int kv0 = w.tile_row();
-      const int lim = p.causal ? min(w.end, q_pos + 1) : w.end;
-      const int nvis = lim - kv0;  // visible keys: a prefix of the tile
+    for (int x = 0; x < n; ++x, w.advance(ring)) {
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        const int kv0 = w.tile_row();
+        const int lim = p.causal ? min(w.end, q_pos + 1) : w.end;
+        const int nvis = lim - kv0;  // visible keys: a prefix of the tile
+        const bool masked = __any_sync(0xffffffffu, nvis < 64 * ch + 64);
+        // Phase 1: P of this half's key columns [64 ch, 64 ch + 64), kept in
+        // registers; then S's region is released for S(x + 1).
+        float pv[64];
 #pragma unroll
-      for (int q = 0; q < kT / 32; ++q) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(row_addr + q * 32, sv);
-        tmem_ld32(row_addr + kT + q * 32, dv);
-        tmem_wait_ld();
-        reg_fence32(sv);
-        reg_fence32(dv);
-        uint32_t dw[16];
+        for (int q = 0; q < 2; ++q) {
+          uint32_t sv[32];
+          tmem_ld32(row_addr + ch * 64 + q * 32, sv);
+          tmem_wait_ld();
+          reg_fence32(sv);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = q * 32 + 2 * e;
-          float p0 = ex2_approx(__uint_as_float(sv[2 * e]) * c2 - lse2);
-          float p1 = ex2_approx(__uint_as_float(sv[2 * e + 1]) * c2 - lse2);
-          if (c0 >= nvis) p0 = 0.f;
-          if (c0 + 1 >= nvis) p1 = 0.f;
-          dw[e] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * e]) - dlt),
-                              p1 * (__uint_as_float(dv[2 * e + 1]) - dlt));
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = ch * 64 + q * 32 + 2 * e;
+            const float2 xs = __ffma2_rn(
+                make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c22, nl);
+            float2 pp = make_float2(ex2_approx(xs.x), ex2_approx(xs.y));
+            if (masked) {
+              if (c0 >= nvis) pp.x = 0.f;
+              if (c0 + 1 >= nvis) pp.y = 0.f;
+            }
+            pv[q * 32 + 2 * e] = pp.x;
+            pv[q * 32 + 2 * e + 1] = pp.y;
+          }
         }
-        tmem_st16(row_addr + q * 16, dw);
+        tc_fence_before();
+        mbar_arrive(p_full);
+        // Phase 2: dS = P (dP - D), stored packed to columns
+        // [64 ch, 64 ch + 32) of the dP region (already read here).
+        ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t dv[32];
+            tmem_ld32(row_addr + kT + ch * 64 + q * 32, dv);
+            tmem_wait_ld();
+            reg_fence32(dv);
+            uint32_t dw[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 ds = __fmul2_rn(
+                  make_float2(pv[q * 32 + 2 * e], pv[q * 32 + 2 * e + 1]),
+                  __fadd2_rn(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd));
+              dw[e] = pack_bf16x2(ds.x, ds.y);
+            }
+            tmem_st16(row_addr + kT + ch * 64 + q * 16, dw);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(ds_full);
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
       if (ok) {
         tc_fence_after();
-        store_row<D>(row_addr + 2 * kT, p.scale, p.dq + ri * D, row_valid);
+        // Warps 0-3 write output columns [0, D/2), warps 4-7 [D/2, D).
+        const uint32_t src = row_addr + 2 * kT + ch * (D / 2);
+        uint4* d4 = reinterpret_cast<uint4*>(p.dq + ri * D + ch * (D / 2));
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q) {
+          uint32_t rr[32];
+          tmem_ld32(src + q * 32, rr);
+          tmem_wait_ld();
+          reg_fence32(rr);
+          uint32_t ww[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            ww[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale,
+                                __uint_as_float(rr[2 * e + 1]) * p.scale);
+          if (row_valid) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[q * 4 + e] = make_uint4(ww[4 * e], ww[4 * e + 1], ww[4 * e + 2], ww[4 * e + 3]);
+          }
+        }
         tc_fence_before();
       }
     }
@@ -821,7 +968,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), C::kTmemCols);
   }
