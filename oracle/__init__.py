@@ -34,6 +34,8 @@ Modules:
   aligned-group first-fit packing into micro-batches) plus brute-force checkers.
 * :mod:`oracle.backward`  -- the attention backward (dQ, dK, dV): the exact
   derivative of the forward's definition, in full and over the ring's blocks.
+* :mod:`oracle.dcp`       -- selecting a micro-batch's samples into a packed
+  array and restoring outputs to the original sample order ([DCP]).
 """
 
-from . import attention, backward, planner  # noqa: F401
+from . import attention, backward, dcp, planner  # noqa: F401
