@@ -49,7 +49,7 @@ def parse_args():
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=[None, "main", "long128k", "merge8", "backward"],
+                    choices=[None, "main", "long128k", "merge8", "backward", "dcp"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -297,9 +297,9 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8", "backward"):
+    if args.only in ("long128k", "merge8", "backward", "dcp"):
         fn = {"long128k": run_long128k, "merge8": run_merge8,
-              "backward": run_backward}[args.only]
+              "backward": run_backward, "dcp": run_dcp_permute}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -428,7 +428,7 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for fn in (run_long128k, run_merge8, run_backward):
+        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute):
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
     clk = clocks.stop()
@@ -565,6 +565,41 @@ def run_backward(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
         torch.cuda.empty_cache()
     return {"backward": {"what": "cpattn_bwd (delta + dK/dV + dQ kernels), inputs resident; "
                                  "FLOPs = 2.5 x forward (5 matmuls over visible pairs)", **sub}}
+
+
+def run_dcp_permute(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                    bf16_sustained, hbm_peak):
+    """cpattn_permute_samples (select of every sample in reversed order, then
+    restore) on a 65,536-token packed batch, H=32, D=128 bf16: HBM bound,
+    bytes = rows x row bytes read + written per call."""
+    H, D = 32, 128
+    lengths = workloads.packed_lengths(args.seed, 65536)
+    T = sum(lengths)
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    x = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+    ids = torch.arange(len(lengths) - 1, -1, -1, dtype=torch.int32, device=dev)
+    pack_cu, status = cpattn.select_cu(cu, ids)
+    packed = torch.empty_like(x)
+    back = torch.empty_like(x)
+    steps = max(10, min(args.steps, 50))
+    res = {}
+    for name, fn in (("select", lambda: cpattn.permute_samples(x, cu, pack_cu, ids, status,
+                                                               gather=True, dst=packed)),
+                     ("restore", lambda: cpattn.permute_samples(packed, cu, pack_cu, ids, status,
+                                                                gather=False, dst=back))):
+        clocks.mark(True)
+        ms = time_loop(torch, fn, steps, 3, stream)
+        clocks.mark(False)
+        nbytes = 2 * T * H * D * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "bytes": nbytes}
+    assert torch.equal(back, x)
+    del x, packed, back
+    torch.cuda.empty_cache()
+    return {"dcp_permute": {"workload": "%d-token packed batch (%d samples), H=32, D=128 bf16, "
+                                        "every sample moved (reversed order)" % (T, len(lengths)),
+                            **res}}
 
 
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,

@@ -263,6 +263,42 @@ int cpattn_bwd(const void* q, const void* k, const void* v, const void* out,
                void* stream);
 
 /*
+ * Dynamic-CP data movement ("Dynamic Context Parallelism (DCP)", verl
+ * documentation: each DPxCP rank selects its assigned samples from the shared
+ * mini-batch; each CP group's output is gathered; verl restores the original
+ * sample order afterwards).  On one device both are permutations of whole
+ * samples between the original packed THD array (samples 0..num_seqs-1 in
+ * original order, cu_seqlens `orig_cu`) and a packed array holding samples
+ * ids[0..n-1] in that order (cu_seqlens `pack_cu`).
+ *
+ * cpattn_select_cu -- pack_cu of a selection: dst_cu[0] = 0,
+ *   dst_cu[i+1] = dst_cu[i] + length of sample ids[i].
+ *   src_cu   device int32 [num_seqs + 1] (original cu_seqlens)
+ *   ids      device int32 [n]; dst_cu device int32 [n + 1] (written)
+ *   status   device int32 [1]: set to 0, or to 1 if an id is outside
+ *            [0, num_seqs) (such a sample counts as empty; the permutation
+ *            below then copies nothing).
+ * cpattn_permute_samples -- copies rows of row_bytes bytes (a multiple of 4;
+ *   16-byte vector copies when it and both buffers allow): gather = 1 copies
+ *   sample ids[i] of the original array `src` to slot i of the packed array
+ *   `dst`; gather = 0 copies slot i of the packed array `src` back to sample
+ *   ids[i] of the original array `dst`.  `status` is the word
+ *   cpattn_select_cu wrote for these ids (nothing is copied when it is
+ *   nonzero).  The packed array holds pack_cu[n] rows; rows of a slot
+ *   beyond its original sample's length are not copied.  Samples not in ids
+ *   are untouched.
+ * Both enqueue on `stream` and return CPATTN_ERR_INVALID_ARG for null or
+ * misaligned pointers and negative sizes before launching.
+ */
+int cpattn_select_cu(const int32_t* src_cu, int32_t num_seqs, const int32_t* ids,
+                     int32_t n, int32_t* dst_cu, int32_t* status, void* stream);
+int cpattn_permute_samples(const void* src, const int32_t* orig_cu,
+                           int32_t num_seqs, const int32_t* pack_cu,
+                           const int32_t* ids, int32_t n, int64_t row_bytes,
+                           int32_t gather, void* dst, const int32_t* status,
+                           void* stream);
+
+/*
  * cpattn_fwd_noalloc -- cpattn_fwd (CPATTN_MODE_FUSED) for callers that cannot
  * allocate device memory.
  *

@@ -62,6 +62,11 @@ _lib.cpattn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, 
                             _i32, _i32, ctypes.c_float, _i32, _vp, _vp, _vp, _vp,
                             ctypes.c_size_t, _vp]
 _lib.cpattn_bwd.restype = ctypes.c_int
+_lib.cpattn_select_cu.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _vp]
+_lib.cpattn_select_cu.restype = ctypes.c_int
+_lib.cpattn_permute_samples.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _vp, _vp,
+                                        _vp]
+_lib.cpattn_permute_samples.restype = ctypes.c_int
 _lib.cpattn_poll_error.argtypes = [_vp, _vp]
 _lib.cpattn_poll_error.restype = ctypes.c_int
 _lib.cpattn_status_string.argtypes = [ctypes.c_int]
@@ -321,6 +326,78 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens, cp_size=None, *, max_seqlen, max_cp
                          _stream(stream))
     _check(st, "cpattn_bwd")
     return tuple(grads)
+
+
+# -------------------------------------------------------- DCP data movement --
+
+def select_cu(cu_seqlens, ids, *, stream=None):
+    """``cpattn_select_cu``: cu_seqlens of the packed selection of samples
+    ``ids`` (device int32).  Returns ``(pack_cu, status)`` (device int32
+    tensors; status 0 when every id is valid)."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    _need(ids, "ids", torch.int32, cu_seqlens.device)
+    n = ids.numel()
+    pack_cu = torch.empty(n + 1, dtype=torch.int32, device=cu_seqlens.device)
+    status = torch.empty(1, dtype=torch.int32, device=cu_seqlens.device)
+    st = _lib.cpattn_select_cu(_ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(ids), n,
+                               _ptr(pack_cu), _ptr(status), _stream(stream))
+    _check(st, "cpattn_select_cu")
+    return pack_cu, status
+
+
+def permute_samples(src, orig_cu, pack_cu, ids, status, *, gather, dst, stream=None):
+    """``cpattn_permute_samples`` on token-major tensors (``[T, ...]``, rows
+    contiguous): ``gather=True`` copies samples ``ids`` of the original
+    ``src`` into the packed ``dst``; ``gather=False`` copies the packed
+    ``src`` back into the original ``dst``."""
+    if src.dtype != dst.dtype or src.shape[1:] != dst.shape[1:]:
+        raise ValueError("src and dst must have the same dtype and row shape")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    row_bytes = src.element_size() * (src[0].numel() if src.shape[0] else dst[0].numel())
+    st = _lib.cpattn_permute_samples(_ptr(src), _ptr(orig_cu), orig_cu.numel() - 1,
+                                     _ptr(pack_cu), _ptr(ids), ids.numel(), int(row_bytes),
+                                     1 if gather else 0, _ptr(dst), _ptr(status),
+                                     _stream(stream))
+    _check(st, "cpattn_permute_samples")
+    return dst
+
+
+def dcp_fwd(q, k, v, cu_seqlens, plan_result, *, max_cp, softmax_scale=None, causal=True,
+            stream=None):
+    """The forward run the dynamic-CP way on one device: for every micro-batch
+    of ``plan_result`` (from :func:`plan` on the same lengths), select its
+    samples into packed arrays (``cpattn_select_cu``, ``cpattn_permute_samples``),
+    run ``cpattn_fwd`` at the planned CP sizes, and restore O and LSE to the
+    original sample order.  Returns ``(out, lse)`` in the original order."""
+    dev = _fwd_common(q, k, v, cu_seqlens, None)
+    T, H, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    mb = np.asarray(plan_result["micro_batch"])
+    order = np.asarray(plan_result["order"])
+    cps = np.asarray(plan_result["cp_size"])
+    lengths = np.diff(cu_seqlens.cpu().numpy())
+    for m in range(int(plan_result["num_micro_batches"])):
+        sel = [int(b) for b in order if mb[b] == m]
+        ids = torch.tensor(sel, dtype=torch.int32, device=dev)
+        pack_cu, status = select_cu(cu_seqlens, ids, stream=stream)
+        rows = int(sum(lengths[b] for b in sel))
+        packed = []
+        for x in (q, k, v):
+            buf = torch.empty((rows, H, D), dtype=x.dtype, device=dev)
+            permute_samples(x, cu_seqlens, pack_cu, ids, status, gather=True, dst=buf,
+                            stream=stream)
+            packed.append(buf)
+        cp_m = torch.tensor([int(cps[b]) for b in sel], dtype=torch.int32, device=dev)
+        o_m, l_m = fwd(*packed, pack_cu, cp_m, max_seqlen=int(max(lengths[b] for b in sel)),
+                       max_cp=max_cp, softmax_scale=softmax_scale, causal=causal,
+                       stream=stream)
+        permute_samples(o_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=out,
+                        stream=stream)
+        permute_samples(l_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=lse,
+                        stream=stream)
+    return out, lse
 
 
 def merge(o_steps, m_steps, l_steps, *, out_o=None, out_m=None, out_l=None, stream=None):
