@@ -36,6 +36,8 @@ Modules:
   derivative of the forward's definition, in full and over the ring's blocks.
 * :mod:`oracle.dcp`       -- selecting a micro-batch's samples into a packed
   array and restoring outputs to the original sample order ([DCP]).
+* :mod:`oracle.decode`    -- decode-time CP: one new token per sequence
+  against its sharded KV cache, with the LSE-form merge of the shards.
 """
 
-from . import attention, backward, dcp, planner  # noqa: F401
+from . import attention, backward, dcp, decode, planner  # noqa: F401
