@@ -49,7 +49,7 @@ def parse_args():
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=[None, "main", "long128k", "merge8", "backward", "dcp"],
+                    choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -297,9 +297,9 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8", "backward", "dcp"):
-        fn = {"long128k": run_long128k, "merge8": run_merge8,
-              "backward": run_backward, "dcp": run_dcp_permute}[args.only]
+    if args.only in ("long128k", "merge8", "backward", "dcp", "decode"):
+        fn = {"long128k": run_long128k, "merge8": run_merge8, "backward": run_backward,
+              "dcp": run_dcp_permute, "decode": run_decode}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -428,7 +428,7 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute):
+        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute, run_decode):
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
     clk = clocks.stop()
@@ -600,6 +600,41 @@ def run_dcp_permute(torch, cpattn, workloads, dev, stream, args, clocks, bf16_pe
     return {"dcp_permute": {"workload": "%d-token packed batch (%d samples), H=32, D=128 bf16, "
                                         "every sample moved (reversed order)" % (T, len(lengths)),
                             **res}}
+
+
+def run_decode(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+               bf16_sustained, hbm_peak):
+    """Decode-time CP (cpattn_decode: shard partials + LSE-form merge): 64
+    sequences with KV caches of uniform length in [4096, 32768], H=32, D=128,
+    decode CP 4.  HBM bound: bytes = the KV cache read once + q + O, LSE and
+    the partials written and read back."""
+    import numpy as np
+    B, H, D, c = 64, 32, 128, 4
+    lengths = [int(x) for x in np.random.default_rng(args.seed).integers(4096, 32769, B)]
+    T = sum(lengths)
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    k = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, H, D), generator=g, device=dev).to(torch.bfloat16)
+    cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(cpattn._lib.cpattn_decode_workspace_size(B, H, D, c), dtype=torch.uint8,
+                     device=dev)
+    fn = lambda: cpattn.decode(q, k, v, cu, cp=c, out=out, lse=lse, workspace=ws)  # noqa: E731
+    steps = max(10, min(args.steps, 50))
+    clocks.mark(True)
+    ms = time_loop(torch, fn, steps, 3, stream)
+    clocks.mark(False)
+    kv_bytes = 2 * T * H * D * 2
+    other = B * H * D * 2 * 2 + B * H * 4 + 2 * c * B * H * (D + 1) * 4
+    gbs = (kv_bytes + other) / (ms * 1e-3) / 1e9
+    del k, v, q, out, lse, ws
+    torch.cuda.empty_cache()
+    return {"decode": {"workload": "64 sequences, KV cache lengths uniform in [4096, 32768] "
+                                   "(%d tokens), H=32, D=128 bf16, decode CP 4" % T,
+                       "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
+                       "bytes": kv_bytes + other}}
 
 
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,

@@ -299,6 +299,47 @@ int cpattn_permute_samples(const void* src, const int32_t* orig_cu,
                            void* stream);
 
 /*
+ * Decode-time context parallelism ("VeRL Backend Parallelism", backend matrix
+ * and vLLM inference section: for the vLLM engines CP means decode context
+ * parallelism, the KV cache of a sequence split over ranks).  One new query
+ * token per sequence attends to every cached key of its sequence; with decode
+ * CP size `cp` the cache of a sequence of length L is cut into cp contiguous
+ * shards of ceil(L / cp) keys, shard s gives the normalised partial
+ * O_s = softmax(scale q K_s^T) V_s with lse_s = ln sum exp(scale q K_s^T)
+ * (an empty shard: O_s = 0, lse_s = -inf), and the partials merge in the LSE
+ * form: LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
+ *
+ *   q      bf16 [num_seqs, H, D] (16-byte aligned): the new tokens
+ *   k, v   bf16 [total_tokens, H, D]: the KV cache, packed by cu_seqlens
+ *   cu_seqlens  device int32 [num_seqs + 1]
+ *   head_dim 64 or 128; 1 <= cp <= 64.
+ *
+ * cpattn_decode_partials -- the shard partials: o_steps float32
+ *   [cp, num_seqs, H, D] (16-byte aligned), lse_steps float32 [cp, num_seqs, H].
+ * cpattn_merge_lse -- the LSE-form merge of `num_steps` normalised partials
+ *   over `rows` rows: out_o float32 [rows, D], out_lse float32 [rows] or NULL.
+ * cpattn_decode -- both: out bf16 [num_seqs, H, D], lse float32 [num_seqs, H]
+ *   or NULL; workspace >= cpattn_decode_workspace_size(...) bytes, 256-byte
+ *   aligned (holds the partials).
+ * All enqueue on `stream`; argument errors return before any launch.
+ */
+size_t cpattn_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                    int32_t head_dim, int32_t cp);
+int cpattn_decode_partials(const void* q, const void* k, const void* v,
+                           const int32_t* cu_seqlens, int32_t num_seqs,
+                           int64_t total_tokens, int32_t num_heads,
+                           int32_t head_dim, float softmax_scale, int32_t cp,
+                           float* o_steps, float* lse_steps, void* stream);
+int cpattn_merge_lse(const float* o_steps, const float* lse_steps,
+                     int32_t num_steps, int64_t rows, int32_t head_dim,
+                     float* out_o, float* out_lse, void* stream);
+int cpattn_decode(const void* q, const void* k, const void* v,
+                  const int32_t* cu_seqlens, int32_t num_seqs,
+                  int64_t total_tokens, int32_t num_heads, int32_t head_dim,
+                  float softmax_scale, int32_t cp, void* out, float* lse,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * cpattn_fwd_noalloc -- cpattn_fwd (CPATTN_MODE_FUSED) for callers that cannot
  * allocate device memory.
  *

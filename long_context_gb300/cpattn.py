@@ -67,6 +67,16 @@ _lib.cpattn_select_cu.restype = ctypes.c_int
 _lib.cpattn_permute_samples.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _i64, _i32, _vp, _vp,
                                         _vp]
 _lib.cpattn_permute_samples.restype = ctypes.c_int
+_lib.cpattn_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+_lib.cpattn_decode_workspace_size.restype = ctypes.c_size_t
+_lib.cpattn_decode_partials.argtypes = [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32,
+                                        ctypes.c_float, _i32, _vp, _vp, _vp]
+_lib.cpattn_decode_partials.restype = ctypes.c_int
+_lib.cpattn_merge_lse.argtypes = [_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp]
+_lib.cpattn_merge_lse.restype = ctypes.c_int
+_lib.cpattn_decode.argtypes = [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_float,
+                               _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.cpattn_decode.restype = ctypes.c_int
 _lib.cpattn_poll_error.argtypes = [_vp, _vp]
 _lib.cpattn_poll_error.restype = ctypes.c_int
 _lib.cpattn_status_string.argtypes = [ctypes.c_int]
@@ -397,6 +407,76 @@ def dcp_fwd(q, k, v, cu_seqlens, plan_result, *, max_cp, softmax_scale=None, cau
                         stream=stream)
         permute_samples(l_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=lse,
                         stream=stream)
+    return out, lse
+
+
+# -------------------------------------------------------------- decode CP --
+
+def _decode_check(q, k, v, cu_seqlens):
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [B, H, D] and k, v [T, H, D]")
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev, k.shape)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev, (q.shape[0] + 1,))
+    if tuple(k.shape[1:]) != tuple(q.shape[1:]):
+        raise ValueError("q and k must share H and D")
+    return dev
+
+
+def decode_partials(q, k, v, cu_seqlens, *, cp, softmax_scale=None, stream=None):
+    """``cpattn_decode_partials``: returns ``(o_steps [cp, B, H, D] fp32,
+    lse_steps [cp, B, H] fp32)``."""
+    dev = _decode_check(q, k, v, cu_seqlens)
+    B, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    o_s = torch.empty((cp, B, H, D), dtype=torch.float32, device=dev)
+    l_s = torch.empty((cp, B, H), dtype=torch.float32, device=dev)
+    st = _lib.cpattn_decode_partials(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B,
+                                     k.shape[0], H, D, float(softmax_scale), int(cp), _ptr(o_s),
+                                     _ptr(l_s), _stream(stream))
+    _check(st, "cpattn_decode_partials")
+    return o_s, l_s
+
+
+def merge_lse(o_steps, lse_steps, *, stream=None):
+    """``cpattn_merge_lse`` over the leading axis of normalised partials
+    ``o_steps [S, ..., D]`` and ``lse_steps [S, ...]``; returns ``(O, LSE)``."""
+    _need(o_steps, "o_steps", torch.float32)
+    _need(lse_steps, "lse_steps", torch.float32, o_steps.device)
+    S, D = o_steps.shape[0], o_steps.shape[-1]
+    rows = lse_steps[0].numel()
+    out = torch.empty(o_steps.shape[1:], dtype=torch.float32, device=o_steps.device)
+    lse = torch.empty(lse_steps.shape[1:], dtype=torch.float32, device=o_steps.device)
+    st = _lib.cpattn_merge_lse(_ptr(o_steps), _ptr(lse_steps), S, rows, D, _ptr(out), _ptr(lse),
+                               _stream(stream))
+    _check(st, "cpattn_merge_lse")
+    return out, lse
+
+
+def decode(q, k, v, cu_seqlens, *, cp, softmax_scale=None, out=None, lse=None, workspace=None,
+           stream=None):
+    """``cpattn_decode``: decode-time CP attention; returns ``(out bf16 [B, H, D],
+    lse fp32 [B, H])``."""
+    dev = _decode_check(q, k, v, cu_seqlens)
+    B, H, D = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        n = _lib.cpattn_decode_workspace_size(B, H, D, int(cp))
+        if n == 0:
+            raise CpattnError(ERR_INVALID_ARG, "cpattn_decode_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    st = _lib.cpattn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, k.shape[0], H, D,
+                            float(softmax_scale), int(cp), _ptr(out), _ptr(lse), _ptr(workspace),
+                            workspace.numel(), _stream(stream))
+    _check(st, "cpattn_decode")
     return out, lse
 
 

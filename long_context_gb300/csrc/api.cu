@@ -425,6 +425,108 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
   return CPATTN_OK;
 }
 
+// ----------------------------------------------------------- decode CP --
+
+extern "C" size_t cpattn_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                               int32_t head_dim, int32_t cp) {
+  if (num_seqs < 0 || num_heads < 1 || cp < 1 || cp > kMaxCp ||
+      (head_dim != 64 && head_dim != 128))
+    return 0;
+  const size_t rows = static_cast<size_t>(cp) * num_seqs * num_heads;
+  return align_up(rows * head_dim * sizeof(float)) + align_up(rows * sizeof(float)) + kAlign;
+}
+
+extern "C" int cpattn_decode_partials(const void* q, const void* k, const void* v,
+                                      const int32_t* cu_seqlens, int32_t num_seqs,
+                                      int64_t total_tokens, int32_t num_heads, int32_t head_dim,
+                                      float softmax_scale, int32_t cp, float* o_steps,
+                                      float* lse_steps, void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || total_tokens >= (int64_t(1) << 31) ||
+      num_heads < 1 || num_heads > 65535 || cp < 1 || cp > kMaxCp)
+    return CPATTN_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return CPATTN_ERR_UNSUPPORTED;
+  if (!(std::isfinite(softmax_scale) && softmax_scale > 0.f)) return CPATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return CPATTN_OK;
+  if (q == nullptr || cu_seqlens == nullptr || o_steps == nullptr || lse_steps == nullptr ||
+      !aligned(q, 16) || !aligned(cu_seqlens, 4) || !aligned(o_steps, 16) ||
+      !aligned(lse_steps, 4))
+    return CPATTN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16)))
+    return CPATTN_ERR_INVALID_ARG;
+  DecodeParams dp;
+  dp.q = static_cast<const __nv_bfloat16*>(q);
+  dp.k = static_cast<const __nv_bfloat16*>(k);
+  dp.v = static_cast<const __nv_bfloat16*>(v);
+  dp.cu_seqlens = cu_seqlens;
+  dp.num_seqs = num_seqs;
+  dp.num_heads = num_heads;
+  dp.cp = cp;
+  dp.total_tokens = total_tokens;
+  dp.scale_log2 = softmax_scale * 1.4426950408889634f;
+  dp.o_steps = o_steps;
+  dp.lse_steps = lse_steps;
+  return launch_decode_partials(dp, head_dim, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CPATTN_OK
+             : CPATTN_ERR_CUDA;
+}
+
+static int merge_lse_common(const float* o_steps, const float* lse_steps, int32_t num_steps,
+                            int64_t rows, int32_t head_dim, float* out_o,
+                            __nv_bfloat16* out_bf16, float* out_lse, cudaStream_t stream) {
+  DeviceInfo dev;
+  const int st = device_info(&dev);
+  if (st != CPATTN_OK) return st;
+  MergeParams mp{};
+  mp.o_steps = o_steps;
+  mp.m_steps = lse_steps;
+  mp.l_steps = nullptr;  // normalised partials: l_s = 1, m_s = lse_s
+  mp.num_steps = num_steps;
+  mp.rows = rows;
+  mp.out_o = out_o;
+  mp.out_bf16 = out_bf16;
+  mp.out_lse = out_lse;
+  return launch_merge(mp, head_dim, out_bf16 != nullptr, dev.num_sms, stream) == cudaSuccess
+             ? CPATTN_OK
+             : CPATTN_ERR_CUDA;
+}
+
+extern "C" int cpattn_merge_lse(const float* o_steps, const float* lse_steps, int32_t num_steps,
+                                int64_t rows, int32_t head_dim, float* out_o, float* out_lse,
+                                void* stream) {
+  if (num_steps < 1 || num_steps > kMaxCp || rows < 0) return CPATTN_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return CPATTN_ERR_UNSUPPORTED;
+  if (rows == 0) return CPATTN_OK;
+  if (o_steps == nullptr || lse_steps == nullptr || out_o == nullptr || !aligned(o_steps, 16) ||
+      !aligned(lse_steps, 4) || !aligned(out_o, 16) || (out_lse && !aligned(out_lse, 4)))
+    return CPATTN_ERR_INVALID_ARG;
+  return merge_lse_common(o_steps, lse_steps, num_steps, rows, head_dim, out_o, nullptr, out_lse,
+                          static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cpattn_decode(const void* q, const void* k, const void* v,
+                             const int32_t* cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                             int32_t num_heads, int32_t head_dim, float softmax_scale, int32_t cp,
+                             void* out, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  const size_t need = cpattn_decode_workspace_size(num_seqs, num_heads, head_dim, cp);
+  if (need == 0) return (head_dim != 64 && head_dim != 128) ? CPATTN_ERR_UNSUPPORTED
+                                                            : CPATTN_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (out == nullptr || !aligned(out, 16))) return CPATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return CPATTN_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, kAlign)) return CPATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return CPATTN_ERR_WORKSPACE_TOO_SMALL;
+  const size_t rows = static_cast<size_t>(cp) * num_seqs * num_heads;
+  float* o_steps = static_cast<float*>(workspace);
+  float* lse_steps = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                              align_up(rows * head_dim * sizeof(float)));
+  int st = cpattn_decode_partials(q, k, v, cu_seqlens, num_seqs, total_tokens, num_heads,
+                                  head_dim, softmax_scale, cp, o_steps, lse_steps, stream);
+  if (st != CPATTN_OK || num_seqs == 0) return st;
+  return merge_lse_common(o_steps, lse_steps, cp, static_cast<int64_t>(num_seqs) * num_heads,
+                          head_dim, nullptr, static_cast<__nv_bfloat16*>(out), lse,
+                          static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int cpattn_poll_error(const void* workspace, void* stream) {
   if (workspace == nullptr) return CPATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

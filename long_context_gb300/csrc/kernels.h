@@ -105,14 +105,14 @@ struct BwdParams {
 struct MergeParams {
   const float* o_steps;
   const float* m_steps;
-  const float* l_steps;
+  const float* l_steps;  // null: every l_s is 1 (normalised partials, m_s = their LSE)
   int num_steps;
   long long rows;       // T * H
   float* out_o;         // public merge: O / l in fp32
   float* out_m;
   float* out_l;
   __nv_bfloat16* out_bf16;  // unfused forward: O / l in bf16
-  float* out_lse;           // unfused forward: m + ln l
+  float* out_lse;           // m + ln l (written when not null)
 };
 
 // Host-side forward arguments and the launch sequence shared by the entry
@@ -148,6 +148,25 @@ int attn_smem_bytes(int D);
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const FwdParams& p, int D,
                         bool partials, long long grid, cudaStream_t stream);
+
+// Decode-time CP partials (decode.cu): q [B, H, D] bf16 (one new token per
+// sequence), the KV cache k, v [T, H, D] bf16 packed by cu_seqlens [B + 1];
+// shard s of sequence b is its keys [s*ceil(L/c), min((s+1)*ceil(L/c), L)).
+// Outputs the normalised partials o_steps [c, B, H, D] and their natural-log
+// LSE lse_steps [c, B, H] (an empty shard: 0 and -inf).
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int* cu_seqlens;
+  int num_seqs, num_heads, cp;
+  long long total_tokens;
+  float scale_log2;
+  float* o_steps;
+  float* lse_steps;
+};
+
+cudaError_t launch_decode_partials(const DecodeParams& p, int D, cudaStream_t stream);
 
 int bwd_smem_bytes(int D);
 

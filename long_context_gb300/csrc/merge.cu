@@ -10,6 +10,8 @@
 // alpha/beta product telescopes to one exp(m_s - m*)).  exp(-inf - x) = 0.
 //
 // Memory layout: O_s [S, rows, D], m_s and l_s [S, rows] (rows = T * H).
+// Normalised partials (decode-time CP) come without l_s: l_s = 1 and m_s is
+// the partial's LSE, which makes this the LSE-form merge.
 // A warp owns 32 consecutive rows: lane r reads m_s and l_s of row r (128-byte
 // coalesced loads per step) and leaves that row's S coefficients w_s / l in
 // shared memory; the warp then walks its rows while the lanes stream each
@@ -61,7 +63,8 @@ __global__ void __launch_bounds__(kMergeThreads)
       float w = 0.f;
       if (have) {
         const float m = __ldg(p.m_steps + static_cast<long long>(s) * rows + my_row);
-        const float ls = __ldg(p.l_steps + static_cast<long long>(s) * rows + my_row);
+        const float ls =
+            p.l_steps ? __ldg(p.l_steps + static_cast<long long>(s) * rows + my_row) : 1.f;
         w = (m == kNegInfM) ? 0.f : expf(m - mstar);
         l += w * ls;
       }
@@ -70,9 +73,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     for (int s = 0; s < S; ++s) coef[s * 32 + lane] *= inv_l;
     if (have) {
-      if (BF16_OUT) {
-        if (p.out_lse) p.out_lse[my_row] = l > 0.f ? mstar + logf(l) : kNegInfM;
-      } else {
+      if (p.out_lse) p.out_lse[my_row] = l > 0.f ? mstar + logf(l) : kNegInfM;
+      if (!BF16_OUT) {
         if (p.out_m) p.out_m[my_row] = mstar;
         if (p.out_l) p.out_l[my_row] = l;
       }

@@ -1,0 +1,88 @@
+"""GPU parity of decode-time CP (cpattn_decode_partials, cpattn_merge_lse,
+cpattn_decode) against oracle/decode.py.
+
+The partials are computed in fp32 from bf16 inputs with fp32 probabilities
+(no bf16 rounding inside), so they are held to fp32 rounding: max |dO_s| <=
+1e-4 and |dlse_s| <= 1e-5 * max(1, |lse_s|).  The merge is fp32 throughout
+(MERGE_ATOL).  The fused call writes bf16 O: the forward's tolerances."""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import MERGE_ATOL, check_attention, default_scale
+from long_context_gb300 import workloads
+from oracle import decode as odc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_gb300 import build as lib_build
+    lib_build.build()
+    from long_context_gb300 import cpattn
+    return cpattn
+
+
+def _inputs(lengths, H, D, seed, std=1.0):
+    T = int(sum(lengths))
+    k, v, _ = workloads.qkv(T, H, D, seed, std)
+    g = torch.Generator().manual_seed(seed + 77)
+    q = (torch.randn((len(lengths), H, D), generator=g) * std).to(torch.bfloat16)
+    cu = workloads.cu_seqlens(lengths)
+    return q, k, v, cu
+
+
+CASES = [
+    ([1000, 1, 0, 37, 4096], 2, 128, 4),
+    ([5, 3, 2, 1], 3, 64, 8),
+    ([2048, 700], 4, 128, 1),
+    ([900, 129, 128, 127], 2, 128, 3),
+]
+
+
+@pytest.mark.parametrize("lengths,H,D,c", CASES)
+def test_partials_merge_and_decode(cp, lengths, H, D, c):
+    q, k, v, cu = _inputs(lengths, H, D, seed=sum(lengths) % 31)
+    scale = default_scale(D)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    cud = torch.from_numpy(cu).cuda()
+    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+    ref_os, ref_ls = odc.shard_partials(qf, kf, vf, cu, c, scale)
+    o_s, l_s = cp.decode_partials(qd, kd, vd, cud, cp=c, softmax_scale=scale)
+    o_s, l_s = o_s.cpu().numpy(), l_s.cpu().numpy()
+    assert np.array_equal(np.isneginf(l_s), np.isneginf(ref_ls))
+    fin = np.isfinite(ref_ls)
+    assert np.max(np.abs(o_s - ref_os)) <= 1e-4
+    assert np.max(np.abs(l_s[fin] - ref_ls[fin]) / np.maximum(1, np.abs(ref_ls[fin]))) <= 1e-5
+    # LSE-form merge of the GPU partials against the oracle's merge of them.
+    mo, ml = cp.merge_lse(torch.from_numpy(o_s).cuda(), torch.from_numpy(l_s).cuda())
+    ref_mo, ref_ml = odc.merge_lse(o_s, l_s)
+    assert np.max(np.abs(mo.cpu().numpy() - ref_mo)) <= MERGE_ATOL
+    mlc = ml.cpu().numpy()
+    assert np.array_equal(np.isneginf(mlc), np.isneginf(ref_ml))
+    f2 = np.isfinite(ref_ml)
+    assert np.max(np.abs(mlc[f2] - ref_ml[f2]) / np.maximum(1, np.abs(ref_ml[f2]))) <= 1e-5
+    # The fused call against the plain definition.
+    out, lse = cp.decode(qd, kd, vd, cud, cp=c, softmax_scale=scale)
+    ref_o, ref_l = odc.decode_attention(qf, kf, vf, cu, scale)
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    empty = np.diff(cu) == 0
+    assert np.all(out[empty] == 0) and np.all(np.isneginf(lse[empty]))
+    check_attention(out[~empty], lse[~empty], ref_o[~empty], ref_l[~empty], "decode")
+
+
+def test_decode_cp_invariance_large_scores(cp):
+    """Scores spread over many powers of two; every CP size gives the same
+    answer (within tolerance) as the plain definition."""
+    lengths, H, D = [3000, 17, 640], 2, 128
+    q, k, v, cu = _inputs(lengths, H, D, seed=5, std=2.5)
+    scale = default_scale(D)
+    ref_o, ref_l = odc.decode_attention(*(workloads.to_f64(x) for x in (q, k, v)), cu, scale)
+    for c in (1, 2, 4, 8, 16):
+        out, lse = cp.decode(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cu).cuda(), cp=c,
+                             softmax_scale=scale)
+        check_attention(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "cp %d" % c)
