@@ -38,6 +38,8 @@ Modules:
   array and restoring outputs to the original sample order ([DCP]).
 * :mod:`oracle.decode`    -- decode-time CP: one new token per sequence
   against its sharded KV cache, with the LSE-form merge of the shards.
+* :mod:`oracle.ulysses`   -- the Ulysses all-to-all as a head-group layout
+  transform, and attention run per head group.
 """
 
-from . import attention, backward, dcp, decode, planner  # noqa: F401
+from . import attention, backward, dcp, decode, planner, ulysses  # noqa: F401
