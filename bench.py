@@ -49,7 +49,8 @@ def parse_args():
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode"],
+                    choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
+                             "ulysses"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -297,9 +298,9 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8", "backward", "dcp", "decode"):
+    if args.only in ("long128k", "merge8", "backward", "dcp", "decode", "ulysses"):
         fn = {"long128k": run_long128k, "merge8": run_merge8, "backward": run_backward,
-              "dcp": run_dcp_permute, "decode": run_decode}[args.only]
+              "dcp": run_dcp_permute, "decode": run_decode, "ulysses": run_ulysses}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -428,7 +429,8 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute, run_decode):
+        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute, run_decode,
+                   run_ulysses):
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
     clk = clocks.stop()
@@ -635,6 +637,58 @@ def run_decode(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                                    "(%d tokens), H=32, D=128 bf16, decode CP 4" % T,
                        "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
                        "bytes": kv_bytes + other}}
+
+
+def run_ulysses(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                bf16_sustained, hbm_peak):
+    """Ulysses layout (cpattn_ulysses_layout) on 131,072 tokens, H=32, D=128
+    bf16, SP 8: bytes = the tensor read once and written once.  And Ulysses
+    attention (Q, K, V to head groups, one forward over the 8 groups of 4
+    heads at the planned CP sizes, O and LSE back) on the packed 16K batch,
+    FLOPs as the forward's."""
+    import numpy as np
+    T, H, D, P = 131072, 32, 128, 8
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    x = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty((P, T, H // P, D), dtype=torch.bfloat16, device=dev)
+    back = torch.empty_like(x)
+    steps = max(10, min(args.steps, 50))
+    res = {}
+    nbytes = 2 * T * H * D * 2
+    for name, fn in (("to_head_groups",
+                      lambda: cpattn.ulysses_layout(x, P, to_head_groups=True, dst=y)),
+                     ("from_head_groups",
+                      lambda: cpattn.ulysses_layout(y, P, to_head_groups=False, dst=back))):
+        clocks.mark(True)
+        ms = time_loop(torch, fn, steps, 3, stream)
+        clocks.mark(False)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "bytes": nbytes}
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))
+    del x, y, back
+    torch.cuda.empty_cache()
+
+    w = workloads.WORKLOADS["packed16k"]
+    lengths = workloads.packed_lengths(args.seed, w["budget"])
+    plan = cpattn.plan(lengths, w["world"], w["limit"], w["max_cp"])
+    cps_l = [int(c) for c in plan["cp_size"]]
+    Tp, Hp, Dp = sum(lengths), w["H"], w["D"]
+    q, k, v = workloads.qkv_device(Tp, Hp, Dp, args.seed, device=dev)
+    cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+    cps = torch.tensor(cps_l, dtype=torch.int32, device=dev)
+    fn = lambda: cpattn.ulysses_fwd(q, k, v, cu, P, cps, max_seqlen=max(lengths),  # noqa: E731
+                                    max_cp=max(cps_l), softmax_scale=1.0 / np.sqrt(Dp))
+    clocks.mark(True)
+    ms = time_loop(torch, fn, max(3, min(args.steps, 20)), 3, stream)
+    clocks.mark(False)
+    tf = attention_flops(lengths, Hp, Dp) / (ms * 1e-3) / 1e12
+    res["attention_packed16k"] = {"ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+                                  "sp": P}
+    del q, k, v
+    torch.cuda.empty_cache()
+    return {"ulysses": {"workload": "layout: 131072 tokens, H=32, D=128 bf16, SP 8; attention: "
+                                    "packed 16K batch (%d tokens), H=32 as 8 groups of 4 heads, "
+                                    "planned CP sizes inside each group" % Tp, **res}}
 
 
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,

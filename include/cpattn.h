@@ -340,6 +340,41 @@ int cpattn_decode(const void* q, const void* k, const void* v,
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Ulysses sequence parallelism ("VeRL Backend Parallelism", the USP section:
+ * verl's ulysses_sequence_parallel_size splits the sequence over the SP group
+ * of a [dp, sp] mesh; an all-to-all before attention gives every rank the
+ * whole sequence for H / P of the heads, and the inverse follows attention).
+ * The sequence shards of the P ranks, concatenated, are the packed [T, H, E]
+ * array, so on one device each all-to-all is a layout transform between
+ *   sequence layout    [T, H, E]
+ *   head-group layout  [P, T, H / P, E]  (group p = heads [p H/P, (p+1) H/P))
+ * where E = head_bytes (2 D for bf16 Q/K/V/O rows, 4 for an fp32 LSE).
+ *
+ * cpattn_ulysses_layout -- to_head_groups = 1: sequence -> head-group layout;
+ *   0: head-group -> sequence layout.  src and dst are device buffers of
+ *   num_tokens * num_heads * head_bytes bytes that must not overlap, 4-byte
+ *   aligned (16-byte aligned buffers with 16-byte multiples of (H / P) E use
+ *   16-byte vector copies).  Requirements: num_heads % sp_size == 0,
+ *   (H / P) * head_bytes a multiple of 4, num_tokens * sp_size < 2^31.
+ *   Bit-exact copy; num_tokens = 0 does nothing.
+ * cpattn_ulysses_seqlens -- the cu_seqlens / cp_size of the head-group layout
+ *   seen as one packed batch of P * num_seqs samples with H / P heads, so that
+ *   a single cpattn_fwd (total tokens P T) runs the attention of every group:
+ *   cu_out[p B + b] = cu_seqlens[b] + p T, cu_out[P B] = cu_seqlens[B] +
+ *   (P - 1) T; cp_out[p B + b] = cp_size[b] (1 when cp_size is NULL; cp_out
+ *   may be NULL).  cu_out holds P B + 1 int32, cp_out P B; all device memory.
+ * Both enqueue on `stream` and return CPATTN_ERR_INVALID_ARG for null,
+ * misaligned or overlapping-by-identity pointers and out-of-range sizes before
+ * launching.
+ */
+int cpattn_ulysses_layout(const void* src, void* dst, int64_t num_tokens,
+                          int32_t num_heads, int64_t head_bytes, int32_t sp_size,
+                          int32_t to_head_groups, void* stream);
+int cpattn_ulysses_seqlens(const int32_t* cu_seqlens, const int32_t* cp_size,
+                           int32_t num_seqs, int64_t num_tokens, int32_t sp_size,
+                           int32_t* cu_out, int32_t* cp_out, void* stream);
+
+/*
  * cpattn_fwd_noalloc -- cpattn_fwd (CPATTN_MODE_FUSED) for callers that cannot
  * allocate device memory.
  *

@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcpattn.so")
 
 SOURCES = ["plan.cpp", "api.cu", "schedule.cu", "merge.cu", "attn_fwd.cu", "attn_bwd.cu",
-           "dcp.cu", "decode.cu", "noalloc.cu"]
+           "dcp.cu", "decode.cu", "noalloc.cu", "ulysses.cu"]
 HEADERS = ["kernels.h", "ptx.cuh", "work.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -77,6 +77,10 @@ _lib.cpattn_merge_lse.restype = ctypes.c_int
 _lib.cpattn_decode.argtypes = [_vp, _vp, _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_float,
                                _i32, _vp, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.cpattn_decode.restype = ctypes.c_int
+_lib.cpattn_ulysses_layout.argtypes = [_vp, _vp, _i64, _i32, _i64, _i32, _i32, _vp]
+_lib.cpattn_ulysses_layout.restype = ctypes.c_int
+_lib.cpattn_ulysses_seqlens.argtypes = [_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp]
+_lib.cpattn_ulysses_seqlens.restype = ctypes.c_int
 _lib.cpattn_poll_error.argtypes = [_vp, _vp]
 _lib.cpattn_poll_error.restype = ctypes.c_int
 _lib.cpattn_status_string.argtypes = [ctypes.c_int]
@@ -407,6 +411,77 @@ def dcp_fwd(q, k, v, cu_seqlens, plan_result, *, max_cp, softmax_scale=None, cau
                         stream=stream)
         permute_samples(l_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=lse,
                         stream=stream)
+    return out, lse
+
+
+# ---------------------------------------------------------------- Ulysses --
+
+def ulysses_layout(src, sp_size, *, to_head_groups, dst=None, stream=None):
+    """``cpattn_ulysses_layout``.  ``to_head_groups=True``: ``src [T, H, ...]``
+    -> ``[P, T, H / P, ...]``; ``False``: ``src [P, T, H / P, ...]`` ->
+    ``[T, H, ...]`` (P = ``sp_size``).  Any dtype; contiguous CUDA tensors."""
+    P = int(sp_size)
+    if src.device.type != "cuda" or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    if to_head_groups:
+        if src.dim() < 2 or src.shape[1] % P != 0:
+            raise ValueError("src must be [T, H, ...] with H divisible by sp_size")
+        T, H, rest = src.shape[0], src.shape[1], tuple(src.shape[2:])
+        shape = (P, T, H // P) + rest
+    else:
+        if src.dim() < 3 or src.shape[0] != P:
+            raise ValueError("src must be [sp_size, T, H / sp_size, ...]")
+        T, H, rest = src.shape[1], P * src.shape[2], tuple(src.shape[3:])
+        shape = (T, H) + rest
+    if dst is None:
+        dst = torch.empty(shape, dtype=src.dtype, device=src.device)
+    elif (tuple(dst.shape) != shape or dst.dtype != src.dtype or dst.device != src.device
+          or not dst.is_contiguous()):
+        raise ValueError("dst must be a contiguous %s tensor of shape %s" % (src.dtype, shape))
+    head_bytes = src.element_size() * int(np.prod(rest, dtype=np.int64))
+    st = _lib.cpattn_ulysses_layout(_ptr(src), _ptr(dst), T, H, head_bytes, P,
+                                    1 if to_head_groups else 0, _stream(stream))
+    _check(st, "cpattn_ulysses_layout")
+    return dst
+
+
+def ulysses_seqlens(cu_seqlens, cp_size, sp_size, num_tokens, *, stream=None):
+    """``cpattn_ulysses_seqlens``: cu_seqlens and cp_size of the head-group
+    layout as one packed batch of ``sp_size * B`` samples."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    dev = cu_seqlens.device
+    B = cu_seqlens.numel() - 1
+    if cp_size is not None:
+        _need(cp_size, "cp_size", torch.int32, dev, (B,))
+    P = int(sp_size)
+    cu_out = torch.empty(P * B + 1, dtype=torch.int32, device=dev)
+    cp_out = torch.empty(P * B, dtype=torch.int32, device=dev)
+    st = _lib.cpattn_ulysses_seqlens(_ptr(cu_seqlens), _ptr(cp_size), B, int(num_tokens), P,
+                                     _ptr(cu_out), _ptr(cp_out), _stream(stream))
+    _check(st, "cpattn_ulysses_seqlens")
+    return cu_out, cp_out
+
+
+def ulysses_fwd(q, k, v, cu_seqlens, sp_size, cp_size=None, *, max_seqlen, max_cp=None,
+                softmax_scale=None, causal=True, stream=None):
+    """Attention the Ulysses way on one device: Q, K, V to the head-group
+    layout, one ``cpattn_fwd`` over all P groups (each group a copy of the
+    batch with H / P heads; ``cp_size`` adds ring CP inside every group),
+    then O and LSE back to the sequence layout.  Returns ``(out, lse)``."""
+    _fwd_common(q, k, v, cu_seqlens, cp_size)
+    T, H, D = q.shape
+    P = int(sp_size)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    grouped = [ulysses_layout(x, P, to_head_groups=True, stream=stream).view(P * T, H // P, D)
+               for x in (q, k, v)]
+    cu_g, cp_g = ulysses_seqlens(cu_seqlens, cp_size, P, T, stream=stream)
+    if max_cp is None:
+        max_cp = 1 if cp_size is None or cp_size.numel() == 0 else int(cp_size.max().item())
+    o_g, l_g = fwd(*grouped, cu_g, cp_g, max_seqlen=max_seqlen, max_cp=max_cp,
+                   softmax_scale=softmax_scale, causal=causal, stream=stream)
+    out = ulysses_layout(o_g.view(P, T, H // P, D), P, to_head_groups=False, stream=stream)
+    lse = ulysses_layout(l_g.view(P, T, H // P), P, to_head_groups=False, stream=stream)
     return out, lse
 
 

@@ -144,3 +144,26 @@ def test_fwd_argument_errors_return_before_launch(cp):
     m.restype = ctypes.c_int
     assert m(p, p, p, 0, 8, 1, 128, p, p, p, None) == 1     # zero steps
     assert m(p, p, p, 2, 8, 1, 80, p, p, p, None) == 2      # head_dim 80
+
+
+def test_ulysses_argument_errors_return_before_launch(cp):
+    lib = ctypes.CDLL(cp.library_path())
+    f = lib.cpattn_ulysses_layout
+    f.argtypes = cp._lib.cpattn_ulysses_layout.argtypes
+    f.restype = ctypes.c_int
+    buf = ctypes.create_string_buffer(4096 + 256)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    a, b = ctypes.c_void_p(base), ctypes.c_void_p(base + 1024)
+    assert f(a, b, 8, 6, 256, 4, 1, None) == 1             # H % P != 0
+    assert f(a, b, 8, 8, 6, 8, 1, None) == 1               # chunk of 6 bytes
+    assert f(a, a, 8, 8, 256, 4, 1, None) == 1             # src == dst
+    assert f(a, b, 8, 8, 256, 4, 2, None) == 1             # bad direction
+    assert f(a, b, 1 << 29, 8, 256, 8, 1, None) == 1       # T * P >= 2^31
+    assert f(ctypes.c_void_p(base + 2), b, 8, 8, 256, 4, 1, None) == 1  # misaligned
+    assert f(None, None, 0, 8, 256, 4, 1, None) == 0       # empty: nothing to do
+    s = lib.cpattn_ulysses_seqlens
+    s.argtypes = cp._lib.cpattn_ulysses_seqlens.argtypes
+    s.restype = ctypes.c_int
+    assert s(a, None, 2, 8, 0, b, None, None) == 1         # sp_size 0
+    assert s(None, None, 2, 8, 2, b, None, None) == 1      # no cu_seqlens
+    assert s(a, None, 2, 1 << 30, 4, b, None, None) == 1   # P T >= 2^31
