@@ -126,6 +126,12 @@ struct Cursor {
   __device__ __forceinline__ bool last() const { return kt == nt - 1; }
 };
 
+// Byte offset of 16-byte chunk c of row r in a tile stored as 64-column
+// halves of 128-byte rows with the 128-byte swizzle (the TMA load layout).
+__device__ __forceinline__ int swizzle128(int r, int c) {
+  return (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
 __device__ __forceinline__ void raise_error(WsHeader* hdr, int code) {
   atomicCAS(&hdr->error, 0, code);
 }
@@ -603,7 +609,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-          uint4* dst = reinterpret_cast<uint4*>(p.out + row_idx * D);
+          // The rows go out through Q tile t's buffer, free now (every MMA
+          // reading it completed before o_done[t]): each thread writes its
+          // row there in the 128-byte-swizzled layout (conflict-free), then
+          // the warp copies its own 32 rows out with D / 8 lanes per row, so
+          // every global store instruction writes whole rows.
+          uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+          fence_proxy_async_smem();
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
@@ -615,10 +627,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 16; ++e)
               w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
                                  __uint_as_float(orr[2 * e + 1]) * inv_l);
-            if (row_valid) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                dst[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(stage + swizzle128(r, q * 4 + e)) =
+                  make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+          __syncwarp();
+          {
+            constexpr int kLpr = D / 8;      // lanes per row: one 16-byte chunk each
+            constexpr int kRpi = 32 / kLpr;  // rows per store instruction
+            const int c = lane % kLpr;
+            const int row_w = (warp & 3) * 32;
+#pragma unroll 4
+            for (int it = 0; it < 32 / kRpi; ++it) {
+              const int rr = row_w + it * kRpi + lane / kLpr;
+              const uint4 val = *reinterpret_cast<const uint4*>(stage + swizzle128(rr, c));
+              const int qp = q0 + t * kBM + rr;
+              if (qp < ring.q_blk_end)
+                *reinterpret_cast<uint4*>(
+                    p.out + (static_cast<size_t>(tok0 + qp) * p.num_heads + h) * D + c * 8) = val;
             }
           }
           if (row_valid && p.lse != nullptr)

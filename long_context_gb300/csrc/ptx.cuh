@@ -95,6 +95,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
 
 // Named barrier `id` over `n` threads (whole warps; every lane of each
 // participating warp executes it).  Not a memory access.
+// Orders this thread's generic-proxy shared-memory accesses with async-proxy
+// (TMA, tensor core) accesses on the other side of the fence.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
