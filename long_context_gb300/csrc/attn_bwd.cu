@@ -213,27 +213,53 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
     tma_load_3d(dst + hf * 16384, map, bar, hf * 64, h, row0, pol);
 }
 
-// One thread's row of a [128 x D] fp32 TMEM accumulator, times `mul`, to bf16
-// in global memory (16-byte stores).
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, __nv_bfloat16* dst,
-                                          bool valid) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+// Byte offset of 16-byte chunk c of row r in a 128-row tile buffer laid out
+// as 64-column halves of 128-byte rows with the 128-byte swizzle (the TMA
+// load layout).
+__device__ __forceinline__ int swizzle128(int r, int c) {
+  return (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Columns [col0, col0 + NC) of this thread's row r of a [128 x D] fp32 TMEM
+// accumulator (TMEM address `taddr` = that row at column col0), times `mul`,
+// to bf16 in global memory, where tile row i starts at g0 + i * ld.  The
+// rows go out through `stage`, a free 128-row tile buffer: each thread writes
+// its row there in the swizzled layout (conflict-free), then the warp copies
+// its own 32 rows (from row0) out with NC / 8 lanes per row, so each store
+// instruction writes whole row segments instead of 16 bytes of 32 rows.
+// Rows i >= n_rows are not written.
+template <int NC>
+__device__ __forceinline__ void store_rows_staged(uint32_t taddr, float mul, uint8_t* stage,
+                                                  int r, int col0, int lane, int row0,
+                                                  __nv_bfloat16* g0, size_t ld, int n_rows) {
+  uint32_t v[NC];
 #pragma unroll
-  for (int q = 0; q < D / 32; ++q) {
-    uint32_t r[32];
-    tmem_ld32(taddr + q * 32, r);
-    tmem_wait_ld();
-    reg_fence32(r);
+  for (int q = 0; q < NC / 32; ++q) tmem_ld32(taddr + q * 32, v + q * 32);
+  tmem_wait_ld();
+#pragma unroll
+  for (int q = 0; q < NC / 32; ++q) reg_fence32(v + q * 32);
+  fence_proxy_async_smem();
+#pragma unroll
+  for (int q = 0; q < NC / 32; ++q) {
     uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e)
-      w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-    if (valid) {
+      w[e] = pack_bf16x2(__uint_as_float(v[q * 32 + 2 * e]) * mul,
+                         __uint_as_float(v[q * 32 + 2 * e + 1]) * mul);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        d4[q * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-    }
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint4*>(stage + swizzle128(r, (col0 + q * 32) / 8 + e)) =
+          make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+  }
+  __syncwarp();
+  constexpr int kLpr = NC / 8;      // lanes per row: one 16-byte chunk each
+  constexpr int kRpi = 32 / kLpr;  // rows per store instruction
+  const int c = col0 / 8 + lane % kLpr;
+#pragma unroll 4
+  for (int it = 0; it < 32 / kRpi; ++it) {
+    const int rr = row0 + it * kRpi + lane / kLpr;
+    const uint4 val = *reinterpret_cast<const uint4*>(stage + swizzle128(rr, c));
+    if (rr < n_rows) *reinterpret_cast<uint4*>(g0 + rr * ld + c * 8) = val;
   }
 }
 
@@ -514,7 +540,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t row_addr = tmem + lane_base;
     const int k_pos = kv0 + r;
-    const bool key_valid = k_pos < kv_blk_end;
     const float c2 = p.scale_log2;
     const float2 c22 = make_float2(c2, c2);
     const int n = count_tiles(ring);
@@ -619,11 +644,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
       if (ok) {
         tc_fence_after();
-        const size_t ri = static_cast<size_t>(u.tok0 + k_pos) * p.num_heads + u.h;
+        // dV goes out through the K buffer, dK through the V buffer (every
+        // MMA reading them has completed).
+        const size_t ri0 = static_cast<size_t>(u.tok0 + kv0) * p.num_heads + u.h;
+        const size_t ld = static_cast<size_t>(p.num_heads) * D;
+        const int n_rows = kv_blk_end - kv0;
         if (ch == 0)
-          store_row<D>(row_addr + 2 * kT, 1.f, p.dv + ri * D, key_valid);
+          store_rows_staged<D>(row_addr + 2 * kT, 1.f, smem + C::kA0Off, r, 0, lane,
+                               (warp & 3) * 32, p.dv + ri0 * D, ld, n_rows);
         else
-          store_row<D>(row_addr + 3 * kT, p.scale, p.dk + ri * D, key_valid);
+          store_rows_staged<D>(row_addr + 3 * kT, p.scale, smem + C::kA1Off, r, 0, lane,
+                               (warp & 3) * 32, p.dk + ri0 * D, ld, n_rows);
         tc_fence_before();
       }
     }
@@ -937,26 +968,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
       if (ok) {
         tc_fence_after();
-        // Warps 0-3 write output columns [0, D/2), warps 4-7 [D/2, D).
-        const uint32_t src = row_addr + 2 * kT + ch * (D / 2);
-        uint4* d4 = reinterpret_cast<uint4*>(p.dq + ri * D + ch * (D / 2));
-#pragma unroll
-        for (int q = 0; q < D / 64; ++q) {
-          uint32_t rr[32];
-          tmem_ld32(src + q * 32, rr);
-          tmem_wait_ld();
-          reg_fence32(rr);
-          uint32_t ww[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            ww[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale,
-                                __uint_as_float(rr[2 * e + 1]) * p.scale);
-          if (row_valid) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[q * 4 + e] = make_uint4(ww[4 * e], ww[4 * e + 1], ww[4 * e + 2], ww[4 * e + 3]);
-          }
-        }
+        // Warps 0-3 write output columns [0, D/2), warps 4-7 [D/2, D), both
+        // through the Q buffer (every MMA reading it has completed).
+        const size_t ri0 = static_cast<size_t>(u.tok0 + q0) * p.num_heads + u.h;
+        store_rows_staged<D / 2>(row_addr + 2 * kT + ch * (D / 2), p.scale, smem + C::kA0Off, r,
+                                 ch * (D / 2), lane, (warp & 3) * 32, p.dq + ri0 * D,
+                                 static_cast<size_t>(p.num_heads) * D, q_blk_end - q0);
         tc_fence_before();
       }
     }

@@ -616,17 +616,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // every global store instruction writes whole rows.
           uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
           fence_proxy_async_smem();
+          // All D columns of the row in flight before one wait.
+          uint32_t orr[D];
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) tmem_ld32(o_addr + q * 32, orr + q * 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) reg_fence32(orr + q * 32);
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
-            uint32_t orr[32];
-            tmem_ld32(o_addr + q * 32, orr);
-            tmem_wait_ld();
-            reg_fence32(orr);
             uint32_t w[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                                 __uint_as_float(orr[2 * e + 1]) * inv_l);
+              w[e] = pack_bf16x2(__uint_as_float(orr[q * 32 + 2 * e]) * inv_l,
+                                 __uint_as_float(orr[q * 32 + 2 * e + 1]) * inv_l);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               *reinterpret_cast<uint4*>(stage + swizzle128(r, q * 4 + e)) =
