@@ -21,9 +21,17 @@
 //              the second 64 columns of each streamed tile
 //   warp  8    TMA producer
 //   warp  9    MMA issuer (one thread) and TMEM owner
-//   warp  10   waits on the hand-offs and releases the MMA warp through named
-//              barrier 1 (the issuing thread never waits on an mbarrier)
+//   warp  10   waits for the streamed tiles' copies
 //   warp  11   idle
+// The MMA warp never waits on an mbarrier (a wait right after
+// tcgen05.commit stalls the tensor queue).  It is released by hardware named
+// barriers: barrier 3 for the first hand-off of each streamed tile and
+// barrier 4 for the second, on which the compute warps arrive (bar.arrive)
+// once their TMEM results are in place and warp 10 once the next tile's copy
+// has landed.  A compute warp whose bounded wait failed switches to bar.sync
+// for its remaining hand-offs, so it cannot arrive twice before a barrier
+// completes, and every warp takes part in every hand-off: the MMA warp always
+// runs to its end.
 //
 // dQ kernel, per 128-query tile, TMEM: S [0,128), dP [128,256), dQ [256,384).
 //   S = Q K^T, dP = dO V^T; dS (bf16 pairs) of key columns [0,64) and
@@ -45,6 +53,8 @@ namespace {
 
 constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;  // warps 0-7
+// Named barriers 3 and 4: the compute warps, warp 10 and the MMA warp.
+constexpr int kHandoffThreads = kComputeThreads + 64;
 constexpr int kT = 128;  // rows of a tile (queries or keys)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInf = __builtin_huge_valf();
@@ -64,9 +74,9 @@ struct BwdCfg {
   // queries, two buffers (float [2][2][128]).
   static constexpr int kVecOff = kB1Off + kStages * kTileBytes;
   static constexpr int kBarOff = kVecOff + 2 * 2 * kT * 4;
-  // a_full, b0_full[S], b0_empty[S], b1_full[S], b1_empty[S], s_full, p_full,
-  // o_done, drain, dp_full, ds_full
-  static constexpr int kNumBars = 1 + 4 * kStages + 6;
+  // a_full, b0_full[S], b0_empty[S], b1_full[S], b1_empty[S], s_full,
+  // o_done, drain, dp_full
+  static constexpr int kNumBars = 1 + 4 * kStages + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
   static constexpr uint32_t kTmemCols = 512;
@@ -263,6 +273,16 @@ __device__ __forceinline__ void store_rows_staged(uint32_t taddr, float mul, uin
   }
 }
 
+// A compute warp's arrival on hand-off barrier `id`: non-blocking while its
+// waits succeed; blocking once one has failed (it then skips its work, and
+// must not run ahead of the barrier).
+__device__ __forceinline__ void handoff(uint32_t id, bool ok) {
+  if (ok)
+    named_bar_arrive(id, kHandoffThreads);
+  else
+    named_bar_sync(id, kHandoffThreads);
+}
+
 struct UnitIds {
   int tok0, L, h, c, rank, blk, chunk;
 };
@@ -345,11 +365,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* b1_full = b0_empty + C::kStages;
   uint64_t* b1_empty = b1_full + C::kStages;
   uint64_t* s_full = b1_empty + C::kStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* o_done = p_full + 1;
+  uint64_t* o_done = s_full + 1;
   uint64_t* drain = o_done + 1;
   uint64_t* dp_full = drain + 1;  // dP^T ready (S^T ready is s_full)
-  uint64_t* ds_full = dp_full + 1;  // dS^T in TMEM (P^T in TMEM is p_full)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
   float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [buf][lse2 | delta][128]
@@ -366,11 +384,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&b1_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kComputeThreads);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, kComputeThreads);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
@@ -466,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int x = 0; x < n; ++x) {
       const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
       const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(1, 64);  // P^T(x) in TMEM; query tile x + 1 landed
+      named_bar_sync(3, kHandoffThreads);  // P^T(x) in TMEM; query tile x + 1 landed
       if (lane == 0) {
         tc_fence_after();
         mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
@@ -476,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       __syncwarp();
-      named_bar_sync(1, 64);  // dS^T(x) in TMEM; dO tile x + 1 landed
+      named_bar_sync(4, kHandoffThreads);  // dS^T(x) in TMEM; dO tile x + 1 landed
       if (lane == 0) {
         tc_fence_after();
         mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
@@ -509,18 +525,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int x = 0; x < n; ++x) {
       const int st1 = (x + 1) % C::kStages;
       const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-      if (lane == 0 && ok) {
-        ok = wait_bounded(p_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-      }
+      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
       __syncwarp();
-      named_bar_sync(1, 64);
-      if (lane == 0 && ok) {
-        ok = wait_bounded(ds_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-      }
+      named_bar_sync(3, kHandoffThreads);
+      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
       __syncwarp();
-      named_bar_sync(1, 64);
+      named_bar_sync(4, kHandoffThreads);
     }
     if (lane == 0 && !ok) {
       raise_error(p.hdr, kErrTimeout);
@@ -563,17 +573,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_bar_sync(2, kComputeThreads);  // the column statistics are in shared memory
       if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+      const float4* lse4 = reinterpret_cast<const float4*>(lse_s);
+      const float4* dlt4 = reinterpret_cast<const float4*>(dlt_s);
+      float pv[64];
       if (ok) {
         tc_fence_after();
         // Causal: query i sees key k_pos iff qt0 + i >= k_pos.
         const int col_lo = p.causal ? max(0, k_pos - qt0) : 0;
         const bool masked = __any_sync(0xffffffffu, col_lo > 64 * ch);
-        const float4* lse4 = reinterpret_cast<const float4*>(lse_s);
-        const float4* dlt4 = reinterpret_cast<const float4*>(dlt_s);
         // Phase 1: P^T of this half's columns [64 ch, 64 ch + 64), kept in
         // registers and stored packed to columns [64 ch, 64 ch + 32) of the
         // S^T region (columns this thread has already read).
-        float pv[64];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           uint32_t sv[32];
@@ -605,10 +615,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_full);
-        // Phase 2: dS^T = P^T (dP^T - D), stored packed over the dP^T region
-        // the same way.
-        ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+      }
+      handoff(3, ok);
+      // Phase 2: dS^T = P^T (dP^T - D), stored packed over the dP^T region
+      // the same way.
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+      {
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -636,9 +648,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(ds_full);
         }
       }
+      handoff(4, ok);
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
@@ -702,11 +714,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* b1_full = b0_empty + C::kStages;
   uint64_t* b1_empty = b1_full + C::kStages;
   uint64_t* s_full = b1_empty + C::kStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* o_done = p_full + 1;
+  uint64_t* o_done = s_full + 1;
   uint64_t* drain = o_done + 1;
   uint64_t* dp_full = drain + 1;   // dP ready (S ready is s_full)
-  uint64_t* ds_full = dp_full + 1;  // dS in TMEM (S read out is p_full)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -722,11 +732,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&b1_empty[st], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kComputeThreads);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, kComputeThreads);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
@@ -822,14 +830,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int x = 0; x < n; ++x) {
       const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
       const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(1, 64);  // S(x) read out; KV tile x + 1's K landed
+      named_bar_sync(3, kHandoffThreads);  // S(x) read out; KV tile x + 1's K landed
       if (lane == 0 && x + 1 < n) {
         tc_fence_after();
         mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
         mma_commit(s_full);
       }
       __syncwarp();
-      named_bar_sync(1, 64);  // dS(x) in TMEM; KV tile x + 1's V landed
+      named_bar_sync(4, kHandoffThreads);  // dS(x) in TMEM; KV tile x + 1's V landed
       if (lane == 0) {
         tc_fence_after();
         mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
@@ -862,18 +870,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int x = 0; x < n; ++x) {
       const int st1 = (x + 1) % C::kStages;
       const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-      if (lane == 0 && ok) {
-        ok = wait_bounded(p_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-      }
+      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
       __syncwarp();
-      named_bar_sync(1, 64);
-      if (lane == 0 && ok) {
-        ok = wait_bounded(ds_full, x & 1, abort_flag);
-        if (ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-      }
+      named_bar_sync(3, kHandoffThreads);
+      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
       __syncwarp();
-      named_bar_sync(1, 64);
+      named_bar_sync(4, kHandoffThreads);
     }
     if (lane == 0 && !ok) {
       raise_error(p.hdr, kErrTimeout);
@@ -906,6 +908,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     w.start(ring);
     for (int x = 0; x < n; ++x, w.advance(ring)) {
       if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+      float pv[64];
       if (ok) {
         tc_fence_after();
         const int kv0 = w.tile_row();
@@ -914,7 +917,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool masked = __any_sync(0xffffffffu, nvis < 64 * ch + 64);
         // Phase 1: P of this half's key columns [64 ch, 64 ch + 64), kept in
         // registers; then S's region is released for S(x + 1).
-        float pv[64];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           uint32_t sv[32];
@@ -936,10 +938,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(p_full);
-        // Phase 2: dS = P (dP - D), stored packed to columns
-        // [64 ch, 64 ch + 32) of the dP region (already read here).
-        ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+      }
+      handoff(3, ok);
+      // Phase 2: dS = P (dP - D), stored packed to columns
+      // [64 ch, 64 ch + 32) of the dP region (already read here).
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(dp_full, x & 1, abort_flag));
+      {
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -960,9 +964,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(ds_full);
         }
       }
+      handoff(4, ok);
     }
     if (ok) {
       ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag));
