@@ -55,6 +55,13 @@ constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;  // warps 0-7
 // Named barriers 3 and 4: the compute warps, warp 10 and the MMA warp.
 constexpr int kHandoffThreads = kComputeThreads + 64;
+// Register split (setmaxnreg): launched at 168 per thread, the compute
+// warpgroups rise to 224 and the control warpgroup drops to 56.
+constexpr int kBwdLaunchRegs = 168;
+constexpr int kBwdSoftmaxRegs = 224;
+constexpr int kBwdCtrlRegs = 56;
+static_assert(kBwdThreads * kBwdLaunchRegs == kComputeThreads * kBwdSoftmaxRegs + 128 * kBwdCtrlRegs,
+              "the register split must add up to the launch total");
 constexpr int kT = 128;  // rows of a tile (queries or keys)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInf = __builtin_huge_valf();
@@ -416,128 +423,145 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 8) {
-    // -------------------------------------------------------- TMA producer --
-    if (lane == 0) {
-      const uint64_t pol_q = l2_policy_evict_last();
-      Walk<KRing> w;
-      w.start(ring);
-      int nb0 = 0, nb1 = 0;
-      if (!w.done(ring)) {
-        nb0 = nb1 = 1;
-        w.advance(ring);
+  static_assert(kBwdSoftmaxRegs == 224 && kBwdCtrlRegs == 56, "immediates below");
+  if (warp >= 8) {
+    regs_lower_56();
+    // Work decoded again after the register split (values live across it
+    // would be spilled there).
+    const UnitIds u = decode(__ldg(&p.table[x_cta]));
+    const int kv0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
+    const int kv_blk_end = min(kv0 + kT, min((u.rank + 1) * u.chunk, u.L));
+    const KRing ring{u.L, u.c, u.chunk, u.rank, p.causal, kv0};
+    if (warp == 8) {
+      // -------------------------------------------------------- TMA producer --
+      if (lane == 0) {
+        const uint64_t pol_q = l2_policy_evict_last();
+        Walk<KRing> w;
+        w.start(ring);
+        int nb0 = 0, nb1 = 0;
+        if (!w.done(ring)) {
+          nb0 = nb1 = 1;
+          w.advance(ring);
+        }
+        bool ok = true;
+        for (; !w.done(ring); w.advance(ring)) {
+          const int x = nb0;
+          const int st = x % C::kStages;
+          const uint32_t ph = (x / C::kStages) & 1;
+          const int row = u.tok0 + w.tile_row();
+          ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
+          load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_q, &b0_full[st], u.h, row, pol_q);
+          ++nb0;
+          ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
+          load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_do, &b1_full[st], u.h, row, pol_q);
+          ++nb1;
+        }
+        if (!ok) {
+          raise_error(p.hdr, kErrTimeout);
+          *abort_flag = 1;
+        }
+        wait_drain(a_full, 0);
+        for (int st = 0; st < C::kStages; ++st) {
+          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
+          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
+        }
       }
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer --
+      const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+      const Desc<D> dsc;
+      const uint32_t k_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
+      const uint32_t v_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
+      const uint32_t q_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
+      const uint32_t do_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
+      const uint32_t q_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
+      const uint32_t do_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB1Off));
+      constexpr uint32_t kStageLo = C::kTileBytes >> 4;
+      const int n = count_tiles(ring);
+      // Two hand-offs per query tile x: once P^T(x) is in TMEM, dV(x) and then
+      // S^T(x + 1) (which overwrites P^T(x) after dV(x) has read it); once
+      // dS^T(x) is in TMEM, dK(x) and then dP^T(x + 1).  The exponentials of
+      // tile x + 1 thus overlap dK(x) and dP^T(x + 1).
+      named_bar_sync(1, 64);  // K, V and query tile 0 landed
+      if (lane == 0 && n > 0) {
+        tc_fence_after();
+        mma_abt<D>(tmem, k_lo, q_lo_k, dsc.hi_k);            // S^T = K Q^T
+        mma_commit(s_full);
+        mma_abt<D>(tmem + kT, v_lo, do_lo_k, dsc.hi_k);      // dP^T = V dO^T
+        mma_commit(dp_full);
+      }
+      __syncwarp();
+      for (int x = 0; x < n; ++x) {
+        const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
+        const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+        named_bar_sync(3, kHandoffThreads);  // P^T(x) in TMEM; query tile x + 1 landed
+        if (lane == 0) {
+          tc_fence_after();
+          mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
+          if (x + 1 < n) {
+            mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_commit(s_full);
+          }
+        }
+        __syncwarp();
+        named_bar_sync(4, kHandoffThreads);  // dS^T(x) in TMEM; dO tile x + 1 landed
+        if (lane == 0) {
+          tc_fence_after();
+          mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
+          mma_commit(&b0_empty[st]);
+          mma_commit(&b1_empty[st]);
+          if (x == n - 1) mma_commit(o_done);
+          if (x + 1 < n) {
+            mma_abt<D>(tmem + kT, v_lo, do_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_commit(dp_full);
+          }
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        mma_commit(drain);
+        wait_drain(drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 10) {
+      // --------------------------------------------- waits for the MMA warp --
+      const int n = count_tiles(ring);
       bool ok = true;
-      for (; !w.done(ring); w.advance(ring)) {
-        const int x = nb0;
-        const int st = x % C::kStages;
-        const uint32_t ph = (x / C::kStages) & 1;
-        const int row = u.tok0 + w.tile_row();
-        ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
-        load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_q, &b0_full[st], u.h, row, pol_q);
-        ++nb0;
-        ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
-        load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_do, &b1_full[st], u.h, row, pol_q);
-        ++nb1;
+      if (lane == 0) {
+        ok = wait_bounded(a_full, 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
       }
-      if (!ok) {
+      __syncwarp();
+      named_bar_sync(1, 64);
+      for (int x = 0; x < n; ++x) {
+        const int st1 = (x + 1) % C::kStages;
+        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+        __syncwarp();
+        named_bar_sync(3, kHandoffThreads);
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        __syncwarp();
+        named_bar_sync(4, kHandoffThreads);
+      }
+      if (lane == 0 && !ok) {
         raise_error(p.hdr, kErrTimeout);
         *abort_flag = 1;
       }
-      wait_drain(a_full, 0);
-      for (int st = 0; st < C::kStages; ++st) {
-        if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
-        if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
-      }
-    }
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer --
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Desc<D> dsc;
-    const uint32_t k_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
-    const uint32_t v_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
-    const uint32_t q_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
-    const uint32_t do_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
-    const uint32_t q_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
-    const uint32_t do_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB1Off));
-    constexpr uint32_t kStageLo = C::kTileBytes >> 4;
-    const int n = count_tiles(ring);
-    // Two hand-offs per query tile x: once P^T(x) is in TMEM, dV(x) and then
-    // S^T(x + 1) (which overwrites P^T(x) after dV(x) has read it); once
-    // dS^T(x) is in TMEM, dK(x) and then dP^T(x + 1).  The exponentials of
-    // tile x + 1 thus overlap dK(x) and dP^T(x + 1).
-    named_bar_sync(1, 64);  // K, V and query tile 0 landed
-    if (lane == 0 && n > 0) {
-      tc_fence_after();
-      mma_abt<D>(tmem, k_lo, q_lo_k, dsc.hi_k);            // S^T = K Q^T
-      mma_commit(s_full);
-      mma_abt<D>(tmem + kT, v_lo, do_lo_k, dsc.hi_k);      // dP^T = V dO^T
-      mma_commit(dp_full);
-    }
-    __syncwarp();
-    for (int x = 0; x < n; ++x) {
-      const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
-      const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(3, kHandoffThreads);  // P^T(x) in TMEM; query tile x + 1 landed
-      if (lane == 0) {
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
-        if (x + 1 < n) {
-          mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
-          mma_commit(s_full);
-        }
-      }
-      __syncwarp();
-      named_bar_sync(4, kHandoffThreads);  // dS^T(x) in TMEM; dO tile x + 1 landed
-      if (lane == 0) {
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
-        mma_commit(&b0_empty[st]);
-        mma_commit(&b1_empty[st]);
-        if (x == n - 1) mma_commit(o_done);
-        if (x + 1 < n) {
-          mma_abt<D>(tmem + kT, v_lo, do_lo_k + st1 * kStageLo, dsc.hi_k);
-          mma_commit(dp_full);
-        }
-      }
       __syncwarp();
     }
-    if (lane == 0) {
-      mma_commit(drain);
-      wait_drain(drain, 0);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // --------------------------------------------- waits for the MMA warp --
-    const int n = count_tiles(ring);
-    bool ok = true;
-    if (lane == 0) {
-      ok = wait_bounded(a_full, 0, abort_flag);
-      if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
-      if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
-    }
-    __syncwarp();
-    named_bar_sync(1, 64);
-    for (int x = 0; x < n; ++x) {
-      const int st1 = (x + 1) % C::kStages;
-      const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-      __syncwarp();
-      named_bar_sync(3, kHandoffThreads);
-      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-      __syncwarp();
-      named_bar_sync(4, kHandoffThreads);
-    }
-    if (lane == 0 && !ok) {
-      raise_error(p.hdr, kErrTimeout);
-      *abort_flag = 1;
-    }
-    __syncwarp();
-  } else if (warp < 8) {
+  } else {
+    regs_raise_224();
+    // Work decoded again after the register split (values live across it
+    // would be spilled there).
+    const UnitIds u = decode(__ldg(&p.table[x_cta]));
+    const int kv0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
+    const int kv_blk_end = min(kv0 + kT, min((u.rank + 1) * u.chunk, u.L));
+    const KRing ring{u.L, u.c, u.chunk, u.rank, p.causal, kv0};
     // -------------------------------------------------------------- compute --
     // Thread r of warps 0-3 and thread r of warps 4-7 own key kv0 + r (TMEM
     // lane r), the first for query columns [0, 64), the second for [64, 128).
@@ -764,125 +788,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  if (warp == 8) {
-    // -------------------------------------------------------- TMA producer --
-    if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      Walk<QRing> w;
-      w.start(ring);
-      int nb0 = 0, nb1 = 0;
-      if (!w.done(ring)) {
-        nb0 = nb1 = 1;
-        w.advance(ring);
+  static_assert(kBwdSoftmaxRegs == 224 && kBwdCtrlRegs == 56, "immediates below");
+  if (warp >= 8) {
+    regs_lower_56();
+    // Work decoded again after the register split (values live across it
+    // would be spilled there).
+    const UnitIds u = decode(__ldg(&p.table[x_cta]));
+    const int q0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
+    const int q_blk_end = min(q0 + kT, min((u.rank + 1) * u.chunk, u.L));
+    const QRing ring{u.L, u.c, u.chunk, u.rank, p.causal, q_blk_end};
+    if (warp == 8) {
+      // -------------------------------------------------------- TMA producer --
+      if (lane == 0) {
+        const uint64_t pol_kv = l2_policy_evict_last();
+        Walk<QRing> w;
+        w.start(ring);
+        int nb0 = 0, nb1 = 0;
+        if (!w.done(ring)) {
+          nb0 = nb1 = 1;
+          w.advance(ring);
+        }
+        bool ok = true;
+        for (; !w.done(ring); w.advance(ring)) {
+          const int x = nb0;
+          const int st = x % C::kStages;
+          const uint32_t ph = (x / C::kStages) & 1;
+          const int row = u.tok0 + w.tile_row();
+          ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
+          load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_k, &b0_full[st], u.h, row, pol_kv);
+          ++nb0;
+          ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
+          load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_v, &b1_full[st], u.h, row, pol_kv);
+          ++nb1;
+        }
+        if (!ok) {
+          raise_error(p.hdr, kErrTimeout);
+          *abort_flag = 1;
+        }
+        wait_drain(a_full, 0);
+        for (int st = 0; st < C::kStages; ++st) {
+          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
+          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
+        }
       }
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer --
+      const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+      const Desc<D> dsc;
+      const uint32_t q_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
+      const uint32_t do_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
+      const uint32_t k_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
+      const uint32_t v_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
+      const uint32_t k_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
+      constexpr uint32_t kStageLo = C::kTileBytes >> 4;
+      const int n = count_tiles(ring);
+      // Two hand-offs per KV tile x: once the compute warps have read S(x),
+      // S(x + 1); once dS(x) is in TMEM (over the dP region), dQ(x) and then
+      // dP(x + 1).  S(x + 1) thus overlaps the dS phase of tile x, and dQ(x),
+      // dP(x + 1) the exponentials of tile x + 1.
+      named_bar_sync(1, 64);  // Q, dO and KV tile 0 landed
+      if (lane == 0 && n > 0) {
+        tc_fence_after();
+        mma_abt<D>(tmem, q_lo, k_lo_k, dsc.hi_k);          // S = Q K^T
+        mma_commit(s_full);
+        mma_abt<D>(tmem + kT, do_lo, v_lo_k, dsc.hi_k);    // dP = dO V^T
+        mma_commit(dp_full);
+        mma_commit(&b1_empty[0]);                          // V consumed
+      }
+      __syncwarp();
+      for (int x = 0; x < n; ++x) {
+        const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
+        const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+        named_bar_sync(3, kHandoffThreads);  // S(x) read out; KV tile x + 1's K landed
+        if (lane == 0 && x + 1 < n) {
+          tc_fence_after();
+          mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_commit(s_full);
+        }
+        __syncwarp();
+        named_bar_sync(4, kHandoffThreads);  // dS(x) in TMEM; KV tile x + 1's V landed
+        if (lane == 0) {
+          tc_fence_after();
+          mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
+          mma_commit(&b0_empty[st]);                                                            // K done
+          if (x == n - 1) mma_commit(o_done);
+          if (x + 1 < n) {
+            mma_abt<D>(tmem + kT, do_lo, v_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_commit(dp_full);
+            mma_commit(&b1_empty[st1]);
+          }
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        mma_commit(drain);
+        wait_drain(drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 10) {
+      // --------------------------------------------- waits for the MMA warp --
+      const int n = count_tiles(ring);
       bool ok = true;
-      for (; !w.done(ring); w.advance(ring)) {
-        const int x = nb0;
-        const int st = x % C::kStages;
-        const uint32_t ph = (x / C::kStages) & 1;
-        const int row = u.tok0 + w.tile_row();
-        ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
-        load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_k, &b0_full[st], u.h, row, pol_kv);
-        ++nb0;
-        ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
-        load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_v, &b1_full[st], u.h, row, pol_kv);
-        ++nb1;
+      if (lane == 0) {
+        ok = wait_bounded(a_full, 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
+        if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
       }
-      if (!ok) {
+      __syncwarp();
+      named_bar_sync(1, 64);
+      for (int x = 0; x < n; ++x) {
+        const int st1 = (x + 1) % C::kStages;
+        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+        __syncwarp();
+        named_bar_sync(3, kHandoffThreads);
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        __syncwarp();
+        named_bar_sync(4, kHandoffThreads);
+      }
+      if (lane == 0 && !ok) {
         raise_error(p.hdr, kErrTimeout);
         *abort_flag = 1;
       }
-      wait_drain(a_full, 0);
-      for (int st = 0; st < C::kStages; ++st) {
-        if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
-        if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
-      }
-    }
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer --
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Desc<D> dsc;
-    const uint32_t q_lo = dsc.lo_k(smem_u32(smem + C::kA0Off));
-    const uint32_t do_lo = dsc.lo_k(smem_u32(smem + C::kA1Off));
-    const uint32_t k_lo_k = dsc.lo_k(smem_u32(smem + C::kB0Off));
-    const uint32_t v_lo_k = dsc.lo_k(smem_u32(smem + C::kB1Off));
-    const uint32_t k_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB0Off));
-    constexpr uint32_t kStageLo = C::kTileBytes >> 4;
-    const int n = count_tiles(ring);
-    // Two hand-offs per KV tile x: once the compute warps have read S(x),
-    // S(x + 1); once dS(x) is in TMEM (over the dP region), dQ(x) and then
-    // dP(x + 1).  S(x + 1) thus overlaps the dS phase of tile x, and dQ(x),
-    // dP(x + 1) the exponentials of tile x + 1.
-    named_bar_sync(1, 64);  // Q, dO and KV tile 0 landed
-    if (lane == 0 && n > 0) {
-      tc_fence_after();
-      mma_abt<D>(tmem, q_lo, k_lo_k, dsc.hi_k);          // S = Q K^T
-      mma_commit(s_full);
-      mma_abt<D>(tmem + kT, do_lo, v_lo_k, dsc.hi_k);    // dP = dO V^T
-      mma_commit(dp_full);
-      mma_commit(&b1_empty[0]);                          // V consumed
-    }
-    __syncwarp();
-    for (int x = 0; x < n; ++x) {
-      const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
-      const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
-      named_bar_sync(3, kHandoffThreads);  // S(x) read out; KV tile x + 1's K landed
-      if (lane == 0 && x + 1 < n) {
-        tc_fence_after();
-        mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
-        mma_commit(s_full);
-      }
-      __syncwarp();
-      named_bar_sync(4, kHandoffThreads);  // dS(x) in TMEM; KV tile x + 1's V landed
-      if (lane == 0) {
-        tc_fence_after();
-        mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
-        mma_commit(&b0_empty[st]);                                                            // K done
-        if (x == n - 1) mma_commit(o_done);
-        if (x + 1 < n) {
-          mma_abt<D>(tmem + kT, do_lo, v_lo_k + st1 * kStageLo, dsc.hi_k);
-          mma_commit(dp_full);
-          mma_commit(&b1_empty[st1]);
-        }
-      }
       __syncwarp();
     }
-    if (lane == 0) {
-      mma_commit(drain);
-      wait_drain(drain, 0);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // --------------------------------------------- waits for the MMA warp --
-    const int n = count_tiles(ring);
-    bool ok = true;
-    if (lane == 0) {
-      ok = wait_bounded(a_full, 0, abort_flag);
-      if (ok && n > 0) ok = wait_bounded(&b0_full[0], 0, abort_flag);
-      if (ok && n > 0) ok = wait_bounded(&b1_full[0], 0, abort_flag);
-    }
-    __syncwarp();
-    named_bar_sync(1, 64);
-    for (int x = 0; x < n; ++x) {
-      const int st1 = (x + 1) % C::kStages;
-      const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
-      __syncwarp();
-      named_bar_sync(3, kHandoffThreads);
-      if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
-      __syncwarp();
-      named_bar_sync(4, kHandoffThreads);
-    }
-    if (lane == 0 && !ok) {
-      raise_error(p.hdr, kErrTimeout);
-      *abort_flag = 1;
-    }
-    __syncwarp();
-  } else if (warp < 8) {
+  } else {
+    regs_raise_224();
+    // Work decoded again after the register split (values live across it
+    // would be spilled there).
+    const UnitIds u = decode(__ldg(&p.table[x_cta]));
+    const int q0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
+    const int q_blk_end = min(q0 + kT, min((u.rank + 1) * u.chunk, u.L));
+    const QRing ring{u.L, u.c, u.chunk, u.rank, p.causal, q_blk_end};
     // -------------------------------------------------------------- compute --
     // Thread r of warps 0-3 and of warps 4-7 own query q0 + r (TMEM lane r),
     // for key columns [0, 64) and [64, 128) of each KV tile:
@@ -1021,6 +1062,11 @@ static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensor
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
                                  const BwdParams& p, long long grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
+  // The register split inside the kernel assumes exactly kBwdLaunchRegs per
+  // thread at launch; with any other count the raise could wait forever.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kBwdLaunchRegs)
+    return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdCfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
