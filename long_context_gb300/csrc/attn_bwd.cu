@@ -67,27 +67,39 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kInf = __builtin_huge_valf();
 constexpr int kErrTimeout = 6;
 
-template <int D>
+// S0 / S1: stages of the rings of streamed tiles B0 / B1; kWithVec: room for
+// the dK/dV kernel's per-tile column statistics.
+template <int D, int S0, int S1, bool kWithVec>
 struct BwdCfg {
   static constexpr int kTileBytes = kT * D * 2;
-  static constexpr int kStages = 2;
+  static constexpr int kStages0 = S0;
+  static constexpr int kStages1 = S1;
   // Stationary tiles A0, A1 (dQ kernel: Q, dO; dK/dV kernel: K, V) and the
   // stage rings B0, B1 of the streamed tiles (dQ: K, V; dK/dV: Q, dO).
   static constexpr int kA0Off = 0;
   static constexpr int kA1Off = kTileBytes;
   static constexpr int kB0Off = 2 * kTileBytes;
-  static constexpr int kB1Off = kB0Off + kStages * kTileBytes;
+  static constexpr int kB1Off = kB0Off + S0 * kTileBytes;
   // dK/dV kernel: per streamed query tile, LSE * log2 e and D of its 128
   // queries, two buffers (float [2][2][128]).
-  static constexpr int kVecOff = kB1Off + kStages * kTileBytes;
-  static constexpr int kBarOff = kVecOff + 2 * 2 * kT * 4;
-  // a_full, b0_full[S], b0_empty[S], b1_full[S], b1_empty[S], s_full,
+  static constexpr int kVecOff = kB1Off + S1 * kTileBytes;
+  static constexpr int kBarOff = kVecOff + (kWithVec ? 2 * 2 * kT * 4 : 0);
+  // a_full, b0_full[S0], b0_empty[S0], b1_full[S1], b1_empty[S1], s_full,
   // o_done, drain, dp_full
-  static constexpr int kNumBars = 1 + 4 * kStages + 4;
+  static constexpr int kNumBars = 1 + 2 * S0 + 2 * S1 + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
 };
+
+// dK/dV: Q and dO each live from their copy to the end of their tile's MMAs.
+template <int D>
+using DkdvCfg = BwdCfg<D, 2, 2, true>;
+// dQ: K is read twice per tile (S = Q K^T, then dQ += dS K), so its stage is
+// freed late; a third K stage gives its copy a full tile period more.
+template <int D>
+using DqCfg = BwdCfg<D, 3, 2, false>;
 
 // Query chunks visited by a stationary query block: the forward's ring (KV
 // chunk (i - s) mod c at step s), restricted to keys below q_blk_end on the
@@ -349,7 +361,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = DkdvCfg<D>;
   const int x_cta = static_cast<int>(blockIdx.x);
   const int n_ctas = __ldcg(&p.hdr->n_items);
   const int err0 = __ldcg(&p.hdr->error);
@@ -368,10 +380,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* a_full = bars;
   uint64_t* b0_full = bars + 1;
-  uint64_t* b0_empty = b0_full + C::kStages;
-  uint64_t* b1_full = b0_empty + C::kStages;
-  uint64_t* b1_empty = b1_full + C::kStages;
-  uint64_t* s_full = b1_empty + C::kStages;
+  uint64_t* b0_empty = b0_full + C::kStages0;
+  uint64_t* b1_full = b0_empty + C::kStages0;
+  uint64_t* b1_empty = b1_full + C::kStages1;
+  uint64_t* s_full = b1_empty + C::kStages1;
   uint64_t* o_done = s_full + 1;
   uint64_t* drain = o_done + 1;
   uint64_t* dp_full = drain + 1;  // dP^T ready (S^T ready is s_full)
@@ -384,9 +396,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 8 && lane == 0) {
     mbar_init(a_full, 1);
-    for (int st = 0; st < C::kStages; ++st) {
+    for (int st = 0; st < C::kStages0; ++st) {
       mbar_init(&b0_full[st], 1);
       mbar_init(&b0_empty[st], 1);
+    }
+    for (int st = 0; st < C::kStages1; ++st) {
       mbar_init(&b1_full[st], 1);
       mbar_init(&b1_empty[st], 1);
     }
@@ -446,18 +460,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (; !w.done(ring); w.advance(ring)) {
           const int x = nb0;
-          const int st = x % C::kStages;
-          const uint32_t ph = (x / C::kStages) & 1;
+          const int st0 = x % C::kStages0;
+          const uint32_t ph0 = (x / C::kStages0) & 1;
+          const int st1 = x % C::kStages1;
+          const uint32_t ph1 = (x / C::kStages1) & 1;
           const int row = u.tok0 + w.tile_row();
-          ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+          ok = wait_bounded(&b0_empty[st0], ph0 ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
-          load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_q, &b0_full[st], u.h, row, pol_q);
+          mbar_arrive_expect_tx(&b0_full[st0], C::kTileBytes);
+          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_q, &b0_full[st0], u.h, row, pol_q);
           ++nb0;
-          ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+          ok = wait_bounded(&b1_empty[st1], ph1 ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
-          load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_do, &b1_full[st], u.h, row, pol_q);
+          mbar_arrive_expect_tx(&b1_full[st1], C::kTileBytes);
+          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_do, &b1_full[st1], u.h, row, pol_q);
           ++nb1;
         }
         if (!ok) {
@@ -465,10 +481,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           *abort_flag = 1;
         }
         wait_drain(a_full, 0);
-        for (int st = 0; st < C::kStages; ++st) {
-          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
-          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
-        }
+        for (int st = 0; st < C::kStages0; ++st)
+          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages0)) & 1);
+        for (int st = 0; st < C::kStages1; ++st)
+          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages1)) & 1);
       }
     } else if (warp == 9) {
       // ---------------------------------------------------------- MMA issuer --
@@ -496,14 +512,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
       for (int x = 0; x < n; ++x) {
-        const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
-        const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+        // Q (ring B0) and dO (ring B1) of tile x and x + 1.
+        const uint32_t q_st = static_cast<uint32_t>(x) % C::kStages0;
+        const uint32_t q_st1 = static_cast<uint32_t>(x + 1) % C::kStages0;
+        const uint32_t do_st = static_cast<uint32_t>(x) % C::kStages1;
+        const uint32_t do_st1 = static_cast<uint32_t>(x + 1) % C::kStages1;
         named_bar_sync(3, kHandoffThreads);  // P^T(x) in TMEM; query tile x + 1 landed
         if (lane == 0) {
           tc_fence_after();
-          mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dV
+          mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + do_st * kStageLo, dsc.hi_mn, x > 0);  // dV
           if (x + 1 < n) {
-            mma_abt<D>(tmem, k_lo, q_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_abt<D>(tmem, k_lo, q_lo_k + q_st1 * kStageLo, dsc.hi_k);
             mma_commit(s_full);
           }
         }
@@ -511,12 +530,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         named_bar_sync(4, kHandoffThreads);  // dS^T(x) in TMEM; dO tile x + 1 landed
         if (lane == 0) {
           tc_fence_after();
-          mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dK
-          mma_commit(&b0_empty[st]);
-          mma_commit(&b1_empty[st]);
+          mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + q_st * kStageLo, dsc.hi_mn, x > 0);  // dK
+          mma_commit(&b0_empty[q_st]);
+          mma_commit(&b1_empty[do_st]);
           if (x == n - 1) mma_commit(o_done);
           if (x + 1 < n) {
-            mma_abt<D>(tmem + kT, v_lo, do_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_abt<D>(tmem + kT, v_lo, do_lo_k + do_st1 * kStageLo, dsc.hi_k);
             mma_commit(dp_full);
           }
         }
@@ -539,12 +558,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       named_bar_sync(1, 64);
       for (int x = 0; x < n; ++x) {
-        const int st1 = (x + 1) % C::kStages;
-        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+        const int st0n = (x + 1) % C::kStages0;
+        const uint32_t ph0n = ((x + 1) / C::kStages0) & 1;
+        const int st1n = (x + 1) % C::kStages1;
+        const uint32_t ph1n = ((x + 1) / C::kStages1) & 1;
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st0n], ph0n, abort_flag);
         __syncwarp();
         named_bar_sync(3, kHandoffThreads);
-        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1n], ph1n, abort_flag);
         __syncwarp();
         named_bar_sync(4, kHandoffThreads);
       }
@@ -715,7 +736,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = DqCfg<D>;
   const int x_cta = static_cast<int>(blockIdx.x);
   const int n_ctas = __ldcg(&p.hdr->n_items);
   const int err0 = __ldcg(&p.hdr->error);
@@ -734,10 +755,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* a_full = bars;
   uint64_t* b0_full = bars + 1;
-  uint64_t* b0_empty = b0_full + C::kStages;
-  uint64_t* b1_full = b0_empty + C::kStages;
-  uint64_t* b1_empty = b1_full + C::kStages;
-  uint64_t* s_full = b1_empty + C::kStages;
+  uint64_t* b0_empty = b0_full + C::kStages0;
+  uint64_t* b1_full = b0_empty + C::kStages0;
+  uint64_t* b1_empty = b1_full + C::kStages1;
+  uint64_t* s_full = b1_empty + C::kStages1;
   uint64_t* o_done = s_full + 1;
   uint64_t* drain = o_done + 1;
   uint64_t* dp_full = drain + 1;   // dP ready (S ready is s_full)
@@ -749,9 +770,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 8 && lane == 0) {
     mbar_init(a_full, 1);
-    for (int st = 0; st < C::kStages; ++st) {
+    for (int st = 0; st < C::kStages0; ++st) {
       mbar_init(&b0_full[st], 1);
       mbar_init(&b0_empty[st], 1);
+    }
+    for (int st = 0; st < C::kStages1; ++st) {
       mbar_init(&b1_full[st], 1);
       mbar_init(&b1_empty[st], 1);
     }
@@ -811,18 +834,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (; !w.done(ring); w.advance(ring)) {
           const int x = nb0;
-          const int st = x % C::kStages;
-          const uint32_t ph = (x / C::kStages) & 1;
+          const int st0 = x % C::kStages0;
+          const uint32_t ph0 = (x / C::kStages0) & 1;
+          const int st1 = x % C::kStages1;
+          const uint32_t ph1 = (x / C::kStages1) & 1;
           const int row = u.tok0 + w.tile_row();
-          ok = wait_bounded(&b0_empty[st], ph ^ 1, abort_flag);
+          ok = wait_bounded(&b0_empty[st0], ph0 ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&b0_full[st], C::kTileBytes);
-          load_tile<D>(smem + C::kB0Off + st * C::kTileBytes, &tm_k, &b0_full[st], u.h, row, pol_kv);
+          mbar_arrive_expect_tx(&b0_full[st0], C::kTileBytes);
+          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_k, &b0_full[st0], u.h, row, pol_kv);
           ++nb0;
-          ok = wait_bounded(&b1_empty[st], ph ^ 1, abort_flag);
+          ok = wait_bounded(&b1_empty[st1], ph1 ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&b1_full[st], C::kTileBytes);
-          load_tile<D>(smem + C::kB1Off + st * C::kTileBytes, &tm_v, &b1_full[st], u.h, row, pol_kv);
+          mbar_arrive_expect_tx(&b1_full[st1], C::kTileBytes);
+          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_v, &b1_full[st1], u.h, row, pol_kv);
           ++nb1;
         }
         if (!ok) {
@@ -830,10 +855,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           *abort_flag = 1;
         }
         wait_drain(a_full, 0);
-        for (int st = 0; st < C::kStages; ++st) {
-          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages)) & 1);
-          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages)) & 1);
-        }
+        for (int st = 0; st < C::kStages0; ++st)
+          if (st < nb0) wait_drain(&b0_full[st], (((nb0 - 1 - st) / C::kStages0)) & 1);
+        for (int st = 0; st < C::kStages1; ++st)
+          if (st < nb1) wait_drain(&b1_full[st], (((nb1 - 1 - st) / C::kStages1)) & 1);
       }
     } else if (warp == 9) {
       // ---------------------------------------------------------- MMA issuer --
@@ -861,25 +886,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
       for (int x = 0; x < n; ++x) {
-        const uint32_t st = static_cast<uint32_t>(x) % C::kStages;
-        const uint32_t st1 = static_cast<uint32_t>(x + 1) % C::kStages;
+        // K (ring B0) and V (ring B1) of tile x and x + 1.
+        const uint32_t k_st = static_cast<uint32_t>(x) % C::kStages0;
+        const uint32_t k_st1 = static_cast<uint32_t>(x + 1) % C::kStages0;
+        const uint32_t v_st1 = static_cast<uint32_t>(x + 1) % C::kStages1;
         named_bar_sync(3, kHandoffThreads);  // S(x) read out; KV tile x + 1's K landed
         if (lane == 0 && x + 1 < n) {
           tc_fence_after();
-          mma_abt<D>(tmem, q_lo, k_lo_k + st1 * kStageLo, dsc.hi_k);
+          mma_abt<D>(tmem, q_lo, k_lo_k + k_st1 * kStageLo, dsc.hi_k);
           mma_commit(s_full);
         }
         __syncwarp();
         named_bar_sync(4, kHandoffThreads);  // dS(x) in TMEM; KV tile x + 1's V landed
         if (lane == 0) {
           tc_fence_after();
-          mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + st * kStageLo, dsc.hi_mn, x > 0);  // dQ
-          mma_commit(&b0_empty[st]);                                                            // K done
+          mma_tmem_a<D>(tmem + 2 * kT, tmem + kT, k_lo_mn + k_st * kStageLo, dsc.hi_mn, x > 0);  // dQ
+          mma_commit(&b0_empty[k_st]);                                                            // K done
           if (x == n - 1) mma_commit(o_done);
           if (x + 1 < n) {
-            mma_abt<D>(tmem + kT, do_lo, v_lo_k + st1 * kStageLo, dsc.hi_k);
+            mma_abt<D>(tmem + kT, do_lo, v_lo_k + v_st1 * kStageLo, dsc.hi_k);
             mma_commit(dp_full);
-            mma_commit(&b1_empty[st1]);
+            mma_commit(&b1_empty[v_st1]);
           }
         }
         __syncwarp();
@@ -901,12 +928,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       named_bar_sync(1, 64);
       for (int x = 0; x < n; ++x) {
-        const int st1 = (x + 1) % C::kStages;
-        const uint32_t ph1 = ((x + 1) / C::kStages) & 1;
-        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st1], ph1, abort_flag);
+        const int st0n = (x + 1) % C::kStages0;
+        const uint32_t ph0n = ((x + 1) / C::kStages0) & 1;
+        const int st1n = (x + 1) % C::kStages1;
+        const uint32_t ph1n = ((x + 1) / C::kStages1) & 1;
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b0_full[st0n], ph0n, abort_flag);
         __syncwarp();
         named_bar_sync(3, kHandoffThreads);
-        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1], ph1, abort_flag);
+        if (lane == 0 && ok && x + 1 < n) ok = wait_bounded(&b1_full[st1n], ph1n, abort_flag);
         __syncwarp();
         named_bar_sync(4, kHandoffThreads);
       }
@@ -1036,9 +1065,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-int bwd_smem_bytes(int D) {
-  return D == 64 ? BwdCfg<64>::kSmemBytes : BwdCfg<128>::kSmemBytes;
-}
 
 cudaError_t launch_bwd_delta(const __nv_bfloat16* out, const __nv_bfloat16* dout,
                              float* delta, long long rows, int D, int num_sms,
@@ -1055,7 +1081,7 @@ cudaError_t launch_bwd_delta(const __nv_bfloat16* out, const __nv_bfloat16* dout
   return cudaGetLastError();
 }
 
-template <int D>
+template <int kSmem>
 static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                                               BwdParams),
                                  const CUtensorMap& tq, const CUtensorMap& tk,
@@ -1067,10 +1093,9 @@ static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensor
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kBwdLaunchRegs)
     return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BwdCfg<D>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), BwdCfg<D>::kSmemBytes, stream>>>(
+  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), kSmem, stream>>>(
       tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
@@ -1078,15 +1103,15 @@ static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensor
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const BwdParams& p, int D, long long grid, cudaStream_t stream) {
-  if (D == 64) return launch_kernel<64>(attn_bwd_dkdv_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
-  return launch_kernel<128>(attn_bwd_dkdv_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
+  if (D == 64) return launch_kernel<DkdvCfg<64>::kSmemBytes>(attn_bwd_dkdv_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
+  return launch_kernel<DkdvCfg<128>::kSmemBytes>(attn_bwd_dkdv_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
 }
 
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo,
                           const BwdParams& p, int D, long long grid, cudaStream_t stream) {
-  if (D == 64) return launch_kernel<64>(attn_bwd_dq_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
-  return launch_kernel<128>(attn_bwd_dq_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
+  if (D == 64) return launch_kernel<DqCfg<64>::kSmemBytes>(attn_bwd_dq_kernel<64>, tq, tk, tv, tdo, p, grid, stream);
+  return launch_kernel<DqCfg<128>::kSmemBytes>(attn_bwd_dq_kernel<128>, tq, tk, tv, tdo, p, grid, stream);
 }
 
 }  // namespace cpattn

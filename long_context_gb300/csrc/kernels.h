@@ -168,7 +168,6 @@ struct DecodeParams {
 
 cudaError_t launch_decode_partials(const DecodeParams& p, int D, cudaStream_t stream);
 
-int bwd_smem_bytes(int D);
 
 // delta[r] = sum_d dO[r, d] * O[r, d] for rows r < rows (= T * H).
 cudaError_t launch_bwd_delta(const __nv_bfloat16* out, const __nv_bfloat16* dout,
