@@ -12,10 +12,12 @@
 // Memory layout: O_s [S, rows, D], m_s and l_s [S, rows] (rows = T * H).
 // Normalised partials (decode-time CP) come without l_s: l_s = 1 and m_s is
 // the partial's LSE, which makes this the LSE-form merge.
-// A warp owns 32 consecutive rows: lane r reads m_s and l_s of row r (128-byte
-// coalesced loads per step) and leaves that row's S coefficients w_s / l in
-// shared memory; the warp then walks its rows while the lanes stream each
-// row's S vectors of D floats as 16-byte loads, 8 steps in flight.
+// A warp owns a chunk of `chunk` consecutive rows (32, 16, 8 or 4, chosen by
+// the host so that the last grid-stride round is nearly full): lane r reads
+// m_s and l_s of row r (coalesced loads per step) and leaves that row's S
+// coefficients w_s / l in shared memory; the warp then walks its rows while
+// the lanes stream each row's S vectors of D floats as 16-byte loads, 8
+// steps in flight.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -35,7 +37,7 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
 
 template <int D, bool BF16_OUT>
 __global__ void __launch_bounds__(kMergeThreads)
-    merge_kernel(const MergeParams p) {
+    merge_kernel(const MergeParams p, int chunk) {
   constexpr int kLanesPerRow = D / 4;          // one float4 per lane
   constexpr int kRowsPerPass = 32 / kLanesPerRow;
   constexpr int kGroup = 8;                    // steps streamed together
@@ -50,10 +52,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int sub = lane / kLanesPerRow;         // row within a pass
   const int col = (lane % kLanesPerRow) * 4;
 
-  for (long long row0 = warp_global * 32; row0 < rows; row0 += nwarps * 32) {
+  for (long long row0 = warp_global * chunk; row0 < rows; row0 += nwarps * chunk) {
     // Row statistics: lane r owns row row0 + r.
     const long long my_row = row0 + lane;
-    const bool have = my_row < rows;
+    const bool have = lane < chunk && my_row < rows;
     float mstar = kNegInfM;
     if (have)
       for (int s = 0; s < S; ++s)
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 
     // Stream the O vectors of the warp's 32 rows, kGroup steps in flight.
 #pragma unroll 2
-    for (int q = 0; q < 32 / kRowsPerPass; ++q) {
+    for (int q = 0; q < chunk / kRowsPerPass; ++q) {
       const int r = q * kRowsPerPass + sub;
       const long long row = row0 + r;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -126,11 +128,31 @@ __global__ void __launch_bounds__(kMergeThreads)
 template <int D, bool BF16_OUT>
 static cudaError_t launch_merge_d(const MergeParams& p, int num_sms,
                                   cudaStream_t stream) {
-  const long long warps_needed = (p.rows + 31) / 32;
-  const long long blocks_needed = (warps_needed * 32 + kMergeThreads - 1) / kMergeThreads;
-  // Grid-stride over at most 8 resident blocks per SM.
+  // Grid-stride over at most 8 resident blocks per SM (the loads in flight
+  // need them all).  Chunk size (a multiple of the rows one pass covers, 1 at
+  // D = 128, 2 at D = 64): the largest of 32, 16, 8, 4 rows whose last
+  // round keeps at least 99 % of the warps busy (U chunks over W warps: the
+  // slowest warp does ceil(U / W) of them against U / W on average).
   const long long cap = static_cast<long long>(num_sms) * 8;
-  const unsigned grid = static_cast<unsigned>(blocks_needed < cap ? blocks_needed : cap);
+  const long long warps_per_block = kMergeThreads / 32;
+  int chunk = 32;
+  long long grid_ll = 0;
+  double best = -1.0;
+  for (int c = 32; c >= 4; c >>= 1) {
+    const long long units = (p.rows + c - 1) / c;
+    const long long b_needed = (units + warps_per_block - 1) / warps_per_block;
+    const long long b = b_needed < cap ? b_needed : cap;
+    const long long w = b * warps_per_block;
+    const long long rounds = (units + w - 1) / w;
+    const double eff = static_cast<double>(units) / static_cast<double>(rounds * w);
+    if (eff > best + 1e-9) {
+      best = eff;
+      chunk = c;
+      grid_ll = b;
+    }
+    if (eff >= 0.99) break;
+  }
+  const unsigned grid = static_cast<unsigned>(grid_ll);
   if (grid == 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(kMergeThreads / 32) * p.num_steps * 32 * sizeof(float);
   auto kern = merge_kernel<D, BF16_OUT>;
@@ -139,7 +161,7 @@ static cudaError_t launch_merge_d(const MergeParams& p, int num_sms,
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kMergeThreads, smem, stream>>>(p);
+  kern<<<grid, kMergeThreads, smem, stream>>>(p, chunk);
   return cudaGetLastError();
 }
 
