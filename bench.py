@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
-                             "ulysses"],
+                             "ulysses", "sweep256"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -298,9 +298,10 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8", "backward", "dcp", "decode", "ulysses"):
+    if args.only in ("long128k", "merge8", "backward", "dcp", "decode", "ulysses", "sweep256"):
         fn = {"long128k": run_long128k, "merge8": run_merge8, "backward": run_backward,
-              "dcp": run_dcp_permute, "decode": run_decode, "ulysses": run_ulysses}[args.only]
+              "dcp": run_dcp_permute, "decode": run_decode, "ulysses": run_ulysses,
+              "sweep256": run_sweep256}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -430,7 +431,7 @@ def main():
     extras = {}
     if not args.no_extras:
         for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute, run_decode,
-                   run_ulysses):
+                   run_ulysses, run_sweep256):
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
     clk = clocks.stop()
@@ -689,6 +690,62 @@ def run_ulysses(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     return {"ulysses": {"workload": "layout: 131072 tokens, H=32, D=128 bf16, SP 8; attention: "
                                     "packed 16K batch (%d tokens), H=32 as 8 groups of 4 heads, "
                                     "planned CP sizes inside each group" % Tp, **res}}
+
+
+def run_sweep256(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                 bf16_sustained, hbm_peak):
+    """The 256-sample sweep: lengths uniform in [256, 32768], planned with
+    cpattn_plan (world 8, limit 4096, CP up to 8); each micro-batch's samples
+    form their own packed THD batch (inputs of every micro-batch resident,
+    distinct data), and one step is the forward of every micro-batch at its
+    planned CP sizes, back to back.  FLOPs as the forward's (4 H D per visible
+    pair)."""
+    import numpy as np
+    w = workloads.WORKLOADS["sweep256"]
+    H, D = w["H"], w["D"]
+    lengths = workloads.uniform_lengths(args.seed, w["n"], w["lo"], w["hi"])
+    plan = cpattn.plan(lengths, w["world"], w["limit"], w["max_cp"])
+    mb = np.asarray(plan["micro_batch"])
+    order = [int(b) for b in plan["order"]]
+    cps_all = np.asarray(plan["cp_size"])
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    batches = []
+    for m in range(int(plan["num_micro_batches"])):
+        ids = [b for b in order if mb[b] == m]
+        lens_m = [lengths[b] for b in ids]
+        T = sum(lens_m)
+        q, k, v = (torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
+                   for _ in range(3))
+        cu = torch.from_numpy(workloads.cu_seqlens(lens_m)).to(dev)
+        cp_m = [int(cps_all[b]) for b in ids]
+        cps = torch.tensor(cp_m, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        ws = cpattn.alloc_workspace(T, len(ids), H, D, max(cp_m), cpattn.MODE_FUSED, device=dev)
+        batches.append((q, k, v, cu, cps, max(lens_m), max(cp_m), out, lse, ws))
+    scale = 1.0 / np.sqrt(D)
+
+    def step():
+        for (q, k, v, cu, cps, max_L, max_c, out, lse, ws) in batches:
+            cpattn.fwd(q, k, v, cu, cps, max_seqlen=max_L, max_cp=max_c, softmax_scale=scale,
+                       out=out, lse=lse, workspace=ws)
+
+    clocks.mark(True)
+    ms = time_loop(torch, step, max(2, min(args.steps, 3)), 2, stream)
+    clocks.mark(False)
+    for b in batches:
+        assert cpattn.poll_error(b[9]) == cpattn.OK
+    flops = attention_flops(lengths, H, D)
+    tf = flops / (ms * 1e-3) / 1e12
+    n_mb = len(batches)
+    del batches
+    torch.cuda.empty_cache()
+    return {"sweep256": {"workload": "256 lengths uniform in [256, 32768] (%d tokens), world 8, "
+                                     "limit 4096, CP up to 8, %d micro-batches from cpattn_plan, "
+                                     "H=32, D=128, causal, bf16 N(0,1)" % (sum(lengths), n_mb),
+                         "ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+                         "frac_of_sustained": tf / bf16_sustained, "flops": flops,
+                         "launches_per_step": 2 * n_mb}}
 
 
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
