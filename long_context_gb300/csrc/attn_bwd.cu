@@ -617,7 +617,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         (ch == 0 ? lse_s : dlt_s)[r] = val;
       }
       named_bar_sync(2, kComputeThreads);  // the column statistics are in shared memory
-      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_full, x & 1, abort_flag));
+#ifdef CPATTN_FAULT_INJECT_DROP_P
+      // Test-only build: in CTA 0, compute warp 0 waits for its first S^T on
+      // the drain barrier, which completes only after the last MMA, so its
+      // bounded wait runs out; the warp then takes part in the remaining
+      // hand-offs with bar.sync, and the kernels end with a timeout status.
+      uint64_t* s_wait = (blockIdx.x == 0 && warp == 0 && x == 0) ? drain : s_full;
+#else
+      uint64_t* s_wait = s_full;
+#endif
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(s_wait, x & 1, abort_flag));
       const float4* lse4 = reinterpret_cast<const float4*>(lse_s);
       const float4* dlt4 = reinterpret_cast<const float4*>(dlt_s);
       float pv[64];
