@@ -150,6 +150,7 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   fp.l_steps = l_steps;
   fp.total_tokens = a.T;
   fp.hdr = hdr;
+  fp.num_sms = dev.num_sms;
   if (launch_attn(tq, tk, tv, fp, a.D, partials, grid, stream) != cudaSuccess)
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;

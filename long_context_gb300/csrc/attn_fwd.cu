@@ -266,6 +266,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_kv = l2_policy_evict_last();
         uint8_t* sk = smem + C::kKOff;
         uint8_t* sv = smem + C::kVOff;
+        // Warm L2 with the Q tiles of CTA x_cta + num_sms, which in table
+        // order starts about when one of the running CTAs ends: its first
+        // copy then reads L2 instead of DRAM.
+        {
+          const int nx = x_cta + p.num_sms;
+          if (nx < n_ctas) {
+            const CtaWork wn = __ldg(&p.table[nx]);
+            const int Ln = wn.y, cn = wn.z & 0xff;
+            const int hn = static_cast<int>(static_cast<unsigned>(wn.z) >> 8);
+            const int rankn = wn.w & 0xff;
+            const int blkn = static_cast<int>(static_cast<unsigned>(wn.w) >> 8);
+            const int chunkn = cdiv(Ln, cn);
+            const int q0n = min(rankn * chunkn, Ln) + blkn * kRowsPerItem;
+            const int qendn = min(q0n + kRowsPerItem, min((rankn + 1) * chunkn, Ln));
+            const int nqn = (q0n + kBM < qendn) ? kNQ : 1;
+            for (int t = 0; t < nqn; ++t)
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_prefetch_l2_3d(&tm_q, hf * 64, hn, wn.x + q0n + t * kBM);
+          }
+        }
         // Q and tile 0 were issued before the CTA barrier.
         Cursor cur;
         cur.start(ring);

@@ -84,6 +84,7 @@ struct FwdParams {
   float* l_steps;
   long long total_tokens;
   WsHeader* hdr;
+  int num_sms;          // CTA x_cta + num_sms is, in table order, a likely next CTA
 };
 
 // Backward kernels (attn_bwd.cu).  Gradients are bf16 [T, H, D]; `lse` is
