@@ -48,6 +48,10 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling aid: the dcp, decode and ulysses measurements on smaller "
+                         "inputs (each array still at least twice the L2 size); not a "
+                         "benchmark configuration")
     ap.add_argument("--only", default=None,
                     choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
                              "ulysses", "sweep256"],
@@ -576,7 +580,7 @@ def run_dcp_permute(torch, cpattn, workloads, dev, stream, args, clocks, bf16_pe
     restore) on a 65,536-token packed batch, H=32, D=128 bf16: HBM bound,
     bytes = rows x row bytes read + written per call."""
     H, D = 32, 128
-    lengths = workloads.packed_lengths(args.seed, 65536)
+    lengths = workloads.packed_lengths(args.seed, 32768 if args.small else 65536)
     T = sum(lengths)
     g = torch.Generator(device=dev).manual_seed(args.seed)
     x = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
@@ -612,7 +616,7 @@ def run_decode(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     decode CP 4.  HBM bound: bytes = the KV cache read once + q + O, LSE and
     the partials written and read back."""
     import numpy as np
-    B, H, D, c = 64, 32, 128, 4
+    B, H, D, c = (8 if args.small else 64), 32, 128, 4
     lengths = [int(x) for x in np.random.default_rng(args.seed).integers(4096, 32769, B)]
     T = sum(lengths)
     g = torch.Generator(device=dev).manual_seed(args.seed)
@@ -634,8 +638,8 @@ def run_decode(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     gbs = (kv_bytes + other) / (ms * 1e-3) / 1e9
     del k, v, q, out, lse, ws
     torch.cuda.empty_cache()
-    return {"decode": {"workload": "64 sequences, KV cache lengths uniform in [4096, 32768] "
-                                   "(%d tokens), H=32, D=128 bf16, decode CP 4" % T,
+    return {"decode": {"workload": "%d sequences, KV cache lengths uniform in [4096, 32768] "
+                                   "(%d tokens), H=32, D=128 bf16, decode CP 4" % (B, T),
                        "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
                        "bytes": kv_bytes + other}}
 
@@ -648,7 +652,8 @@ def run_ulysses(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     heads at the planned CP sizes, O and LSE back) on the packed 16K batch,
     FLOPs as the forward's."""
     import numpy as np
-    T, H, D, P = 131072, 32, 128, 8
+    T_lay, H, D, P = (65536 if args.small else 131072), 32, 128, 8
+    T = T_lay
     g = torch.Generator(device=dev).manual_seed(args.seed)
     x = torch.randn((T, H, D), generator=g, device=dev).to(torch.bfloat16)
     y = torch.empty((P, T, H // P, D), dtype=torch.bfloat16, device=dev)
@@ -687,9 +692,9 @@ def run_ulysses(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                                   "sp": P}
     del q, k, v
     torch.cuda.empty_cache()
-    return {"ulysses": {"workload": "layout: 131072 tokens, H=32, D=128 bf16, SP 8; attention: "
+    return {"ulysses": {"workload": "layout: %d tokens, H=32, D=128 bf16, SP 8; attention: "
                                     "packed 16K batch (%d tokens), H=32 as 8 groups of 4 heads, "
-                                    "planned CP sizes inside each group" % Tp, **res}}
+                                    "planned CP sizes inside each group" % (T_lay, Tp), **res}}
 
 
 def run_sweep256(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
