@@ -139,3 +139,30 @@ def test_backward_packed16k_rows_and_identities(cp):
         sum_dk = dk[s0:s1].astype(np.float64).sum(0)
         scale_dk = np.sqrt((dk[s0:s1].astype(np.float64) ** 2).sum(0)) + 1e-30
         assert np.max(np.abs(sum_dk) / scale_dk) < 0.05, b
+
+
+def test_backward_long128k_rows_and_identities(cp):
+    """The 131,072-token sequence at CP 4 (H=16, D=128, N(0, 0.5^2)): the
+    size and launch configuration the benchmark times.  dQ rows at the chunk
+    edges and at random positions against the oracle (each row computed on
+    its own), and per head sum_j dV_j = sum_i dO_i, sum_j dK_j = 0."""
+    w = workloads.WORKLOADS["long128k"]
+    H, D, L, c = w["H"], w["D"], w["lengths"][0], w["cp"]
+    q, k, v = workloads.qkv(L, H, D, 0, std=w["std"])
+    g = torch.Generator().manual_seed(1000)
+    do = torch.randn((L, H, D), generator=g).to(torch.bfloat16)
+    cu = workloads.cu_seqlens([L])
+    scale = default_scale(D)
+    dq, dk, dv = _fwd_bwd(cp, q, k, v, do, cu, [c], True, scale)
+    chunk = L // c
+    toks = [0, 1, 127, 128] + [j * chunk + d for j in range(1, c) for d in (-1, 0)] + [L - 1]
+    toks += [int(t) for t in np.random.default_rng(7).integers(0, L, 3)]
+    ref_dq, _, _ = ob.backward_rows(q, k, v, do, cu, scale, toks)
+    check_grad(dq[toks], ref_dq, "long128k dq rows")
+    dof = do.float().numpy().astype(np.float64)
+    sum_dv = dv.astype(np.float64).sum(0)
+    scale_dv = np.sqrt((dv.astype(np.float64) ** 2).sum(0)) + 1e-30
+    assert np.max(np.abs(sum_dv - dof.sum(0)) / scale_dv) < 0.05
+    sum_dk = dk.astype(np.float64).sum(0)
+    scale_dk = np.sqrt((dk.astype(np.float64) ** 2).sum(0)) + 1e-30
+    assert np.max(np.abs(sum_dk) / scale_dk) < 0.05
