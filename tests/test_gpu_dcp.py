@@ -92,3 +92,28 @@ def test_dcp_forward_matches_attention(cp):
     check_attention(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "dcp forward")
     full_o, full_l = oa.full_attention(*(workloads.to_f64(x) for x in (q, k, v)), cu, scale)
     assert np.max(np.abs(ref_o - full_o)) < 1e-12
+
+
+def test_select_restore_full_size(cp):
+    """The size the benchmark times: the 65,536-token packed batch, H=32,
+    D=128 bf16, every sample moved in reversed order; the whole packed array
+    against the oracle's selection (bit-exact), then restored bit for bit."""
+    H, D = 32, 128
+    lengths = workloads.packed_lengths(0, 65536)
+    T = sum(lengths)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn((T, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    cu = workloads.cu_seqlens(lengths)
+    ids = list(range(len(lengths) - 1, -1, -1))
+    dcu = torch.from_numpy(cu).cuda()
+    dids = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    pack_cu, status = cp.select_cu(dcu, dids)
+    assert int(status.item()) == 0
+    packed = torch.empty_like(x)
+    cp.permute_samples(x, dcu, pack_cu, dids, status, gather=True, dst=packed)
+    want, want_cu = od.select(x.cpu().view(torch.int16).numpy(), cu, ids)
+    assert np.array_equal(pack_cu.cpu().numpy(), want_cu)
+    assert np.array_equal(packed.cpu().view(torch.int16).numpy(), want)
+    back = torch.empty_like(x)
+    cp.permute_samples(packed, dcu, pack_cu, dids, status, gather=False, dst=back)
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))

@@ -86,3 +86,29 @@ def test_decode_cp_invariance_large_scores(cp):
         out, lse = cp.decode(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cu).cuda(), cp=c,
                              softmax_scale=scale)
         check_attention(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "cp %d" % c)
+
+
+def test_decode_full_size_sampled(cp):
+    """The size the benchmark times: 64 sequences with KV caches of uniform
+    length in [4096, 32768] (about 1.2 M cached tokens, 9.8 GB), H=32, D=128,
+    decode CP 4.  Every sequence's output on the GPU; eight sampled sequences
+    (the shortest, the longest and six more) against the oracle."""
+    B, H, D, c = 64, 32, 128, 4
+    lengths = [int(x) for x in np.random.default_rng(0).integers(4096, 32769, B)]
+    T = sum(lengths)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    k = torch.randn((T, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((T, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((B, H, D), generator=g, device="cuda").to(torch.bfloat16)
+    cu = workloads.cu_seqlens(lengths)
+    scale = default_scale(D)
+    out, lse = cp.decode(q, k, v, torch.from_numpy(cu).cuda(), cp=c, softmax_scale=scale)
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    picks = sorted({int(np.argmin(lengths)), int(np.argmax(lengths))}
+                   | {int(b) for b in np.random.default_rng(3).choice(B, 6, replace=False)})
+    for b in picks:
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        ref_o, ref_l = odc.decode_attention(
+            workloads.to_f64(q[b:b + 1].cpu()), workloads.to_f64(k[s0:s1].cpu()),
+            workloads.to_f64(v[s0:s1].cpu()), [0, s1 - s0], scale)
+        check_attention(out[b:b + 1], lse[b:b + 1], ref_o, ref_l, "sequence %d" % b)
