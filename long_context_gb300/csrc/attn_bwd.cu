@@ -362,6 +362,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using C = DkdvCfg<D>;
+  // Programmatic dependent of the schedule kernel: wait for its table, then
+  // let the dQ kernel (independent of this one) start launching.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int x_cta = static_cast<int>(blockIdx.x);
   const int n_ctas = __ldcg(&p.hdr->n_items);
   const int err0 = __ldcg(&p.hdr->error);
@@ -750,8 +754,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int n_ctas = __ldcg(&p.hdr->n_items);
   const int err0 = __ldcg(&p.hdr->error);
   const CtaWork work = __ldg(&p.table[x_cta]);
-  if (x_cta >= n_ctas) return;
-  if (err0 == kErrTimeout) return;
+  // Programmatic dependent of the dK/dV kernel, which it does not read: it
+  // starts while dK/dV's last CTAs run, and every CTA waits for dK/dV before
+  // it exits, so the backward completes only when both have.
+  if (x_cta >= n_ctas || err0 == kErrTimeout) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
 
   const UnitIds u = decode(work);
   const int q0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
@@ -1072,6 +1081,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(*reinterpret_cast<volatile uint32_t*>(tmem_slot), C::kTmemCols);
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 
@@ -1104,9 +1114,17 @@ static cudaError_t launch_kernel(void (*kern)(CUtensorMap, CUtensorMap, CUtensor
     return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), kSmem, stream>>>(
-      tq, tk, tv, tdo, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, p);
 }
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk,

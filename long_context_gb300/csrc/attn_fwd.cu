@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const FwdParams p) {
   using C = Cfg<D>;
+  // Launched as a programmatic dependent of the schedule kernel: wait for
+  // its table (a no-op when launched normally).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // The three loads are independent, so they are in flight together.  The
   // table holds an entry for every CTA of the grid (used or not).
   const int x_cta = static_cast<int>(blockIdx.x);
@@ -710,9 +713,17 @@ static cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk,
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(static_cast<unsigned>(grid)), dim3(kThreads), Cfg<D>::kSmemBytes,
-         stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,

@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(kSchedThreads)
   __shared__ long long s_carry;
   __shared__ long long warp_sums[32];
   __shared__ int hist[kBuckets];
+  // The attention kernel (launched with programmatic stream serialization)
+  // may start launching now; it waits for this grid's results before use.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   if (tid == 0) {
     s_bad = 0;
