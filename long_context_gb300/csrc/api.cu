@@ -136,6 +136,11 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
       make_qkv_map(&tk, a.k, a.T, a.H, a.D) != CPATTN_OK ||
       make_qkv_map(&tv, a.v, a.T, a.H, a.D) != CPATTN_OK)
     return CPATTN_ERR_CUDA;
+  // O in the same layout (the fused epilogue stores full tiles with TMA);
+  // the partials mode writes no O here, and takes Q's map as a placeholder.
+  CUtensorMap to = tq;
+  if (!partials && out != nullptr && make_qkv_map(&to, out, a.T, a.H, a.D) != CPATTN_OK)
+    return CPATTN_ERR_CUDA;
 
   FwdParams fp;
   fp.table = sp.table;
@@ -151,7 +156,7 @@ int run_attention(const FwdArgs& a, bool partials, int32_t num_steps,
   fp.total_tokens = a.T;
   fp.hdr = hdr;
   fp.num_sms = dev.num_sms;
-  if (launch_attn(tq, tk, tv, fp, a.D, partials, grid, stream) != cudaSuccess)
+  if (launch_attn(tq, tk, tv, to, fp, a.D, partials, grid, stream) != cudaSuccess)
     return CPATTN_ERR_CUDA;
   return CPATTN_OK;
 }

@@ -67,8 +67,8 @@ struct Cfg {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[NQ],
-  // p_full[NQ], o_done[NQ], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kNQ + 1;
+  // p_full[NQ], o_done[NQ], drain, staged[NQ]
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kNQ + 1 + kNQ;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + align slack
   static constexpr uint32_t kTmemCols = 512;
@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p) {
   using C = Cfg<D>;
   // Launched as a programmatic dependent of the schedule kernel: wait for
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + kNQ;
   uint64_t* o_done = p_full + kNQ;
   uint64_t* drain = o_done + kNQ;
+  uint64_t* staged = drain + 1;  // O tile t staged in shared memory (128 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
+    for (int t = 0; t < kNQ; ++t) mbar_init(&staged[t], kBM);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_q);
@@ -646,20 +649,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) reg_fence32(orr + q * 32);
+          const float2 il2 = make_float2(inv_l, inv_l);
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(orr[q * 32 + 2 * e]) * inv_l,
-                                 __uint_as_float(orr[q * 32 + 2 * e + 1]) * inv_l);
+            for (int e = 0; e < 16; ++e) {
+              const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(orr[q * 32 + 2 * e]),
+                                                       __uint_as_float(orr[q * 32 + 2 * e + 1])),
+                                           il2);
+              w[e] = pack_bf16x2(o2.x, o2.y);
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               *reinterpret_cast<uint4*>(stage + swizzle128(r, q * 4 + e)) =
                   make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
-          __syncwarp();
-          {
+          if (q0 + t * kBM + kBM <= ring.q_blk_end) {
+            // A full tile: the staged layout is the TMA layout, so one thread
+            // stores it with the bulk engine once every row is staged (each
+            // thread makes its writes visible to the async proxy first).  The
+            // issuing thread waits only until the engine has read shared
+            // memory, before the CTA's final barrier.
+            fence_proxy_async_smem();
+            mbar_arrive(&staged[t]);
+            if ((warp & 3) == 0 && lane == 0) {
+              if (wait_bounded(&staged[t], 0, abort_flag)) {
+#pragma unroll
+                for (int hf = 0; hf < C::kHalves; ++hf)
+                  tma_store_3d(&tm_o, stage + hf * 16384, hf * 64, h, tok0 + q0 + t * kBM);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+              } else {
+                ok = false;
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+          } else {
+            // The tile that ends a chunk: its rows past the chunk belong to
+            // another rank or sample, so the warp copies its own 32 rows out
+            // with D / 8 lanes per row (every store instruction writes whole
+            // rows), skipping those.
+            __syncwarp();
             constexpr int kLpr = D / 8;      // lanes per row: one 16-byte chunk each
             constexpr int kRpi = 32 / kLpr;  // rows per store instruction
             const int c = lane % kLpr;
@@ -700,7 +731,8 @@ int attn_smem_bytes(int D) {
 
 template <int D, bool PARTIALS>
 static cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk,
-                                 const CUtensorMap& tv, const FwdParams& p,
+                                 const CUtensorMap& tv, const CUtensorMap& to,
+                                 const FwdParams& p,
                                  long long grid, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, PARTIALS>;
   // The register split inside the kernel assumes exactly kLaunchRegs per
@@ -723,18 +755,18 @@ static cudaError_t launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const FwdParams& p, int D,
+                        const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int D,
                         bool partials, long long grid, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (D == 64)
-    return partials ? launch_attn_t<64, true>(tq, tk, tv, p, grid, stream)
-                    : launch_attn_t<64, false>(tq, tk, tv, p, grid, stream);
-  return partials ? launch_attn_t<128, true>(tq, tk, tv, p, grid, stream)
-                  : launch_attn_t<128, false>(tq, tk, tv, p, grid, stream);
+    return partials ? launch_attn_t<64, true>(tq, tk, tv, to, p, grid, stream)
+                    : launch_attn_t<64, false>(tq, tk, tv, to, p, grid, stream);
+  return partials ? launch_attn_t<128, true>(tq, tk, tv, to, p, grid, stream)
+                  : launch_attn_t<128, false>(tq, tk, tv, to, p, grid, stream);
 }
 
 }  // namespace cpattn

@@ -147,7 +147,7 @@ cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 int attn_smem_bytes(int D);
 
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const FwdParams& p, int D,
+                        const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int D,
                         bool partials, long long grid, cudaStream_t stream);
 
 // Decode-time CP partials (decode.cu): q [B, H, D] bf16 (one new token per
