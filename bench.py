@@ -49,9 +49,9 @@ def parse_args():
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true",
-                    help="profiling aid: the dcp, decode and ulysses measurements on smaller "
-                         "inputs (each array still at least twice the L2 size); not a "
-                         "benchmark configuration")
+                    help="profiling aid: the long-sequence (one 32768-token sequence), dcp, "
+                         "decode and ulysses measurements on smaller inputs (each array still "
+                         "larger than L2); not a benchmark configuration")
     ap.add_argument("--only", default=None,
                     choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
                              "ulysses", "sweep256"],
@@ -502,6 +502,8 @@ def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     # 131,072-token causal sequence at CP=4, fused and unfused.
     w = workloads.WORKLOADS["long128k"]
     H, D, L, c = w["H"], w["D"], w["lengths"][0], w["cp"]
+    if args.small:
+        L = 32768  # Q/K/V 134 MB each, still larger than L2
     q, k, v = workloads.qkv_device(L, H, D, args.seed, std=w["std"], device=dev)
     cu = torch.tensor([0, L], dtype=torch.int32, device=dev)
     cps = torch.tensor([c], dtype=torch.int32, device=dev)
@@ -522,8 +524,8 @@ def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
         sub[name] = {"ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
                      "frac_of_sustained": tf / bf16_sustained}
         del ws
-    res["long128k"] = {"workload": "one causal 131072-token sequence, CP=4 (32768-token chunks), "
-                                   "H=16, D=128, bf16 N(0,0.5^2)",
+    res["long128k"] = {"workload": "one causal %d-token sequence, CP=4 (%d-token chunks), "
+                                   "H=16, D=128, bf16 N(0,0.5^2)" % (L, L // c),
                        "flops": flops, "steps": steps, **sub}
     del q, k, v, out, lse
     torch.cuda.empty_cache()
