@@ -94,6 +94,23 @@ def test_empty_samples(cp, mode):
     check_attention(out, lse, ref_o, ref_lse, "empty samples")
 
 
+@pytest.mark.parametrize("n_seqs", [2048, 2500])
+def test_many_samples(cp, n_seqs):
+    """Thousands of short samples (empty ones included) at CP sizes 1-8 in
+    one batch: the schedule kernel's sort and table fill over many samples,
+    every output element against the oracle."""
+    rng = np.random.default_rng(n_seqs)
+    lengths = [int(x) for x in rng.integers(0, 40, n_seqs)]
+    cps = [int(x) for x in rng.choice([1, 2, 4, 8], n_seqs)]
+    H, D = 2, 64
+    (q, k, v, cu), g = make_batch(lengths, H, D, seed=n_seqs)
+    scale = default_scale(D)
+    out, lse = _run(cp, g, lengths, cps, H, D, True, 0, scale)
+    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+    ref_o, ref_lse = oa.full_attention(qf, kf, vf, cu, scale)
+    check_attention(out, lse, ref_o, ref_lse, "%d samples" % n_seqs)
+
+
 def test_zero_tokens(cp):
     H, D = 2, 64
     q = torch.empty((0, H, D), dtype=torch.bfloat16, device="cuda")
