@@ -49,9 +49,10 @@ def parse_args():
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true",
-                    help="profiling aid: the long-sequence (one 32768-token sequence), dcp, "
-                         "decode and ulysses measurements on smaller inputs (each array still "
-                         "larger than L2); not a benchmark configuration")
+                    help="profiling aid: the long-sequence forward and backward (one "
+                         "32768-token sequence), dcp, decode and ulysses measurements on "
+                         "smaller inputs (each array still larger than L2); not a benchmark "
+                         "configuration")
     ap.add_argument("--only", default=None,
                     choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
                              "ulysses", "sweep256"],
@@ -549,6 +550,8 @@ def run_backward(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
             std, steps = 1.0, max(3, min(args.steps, 20))
         else:
             lengths, cps_l, std = list(w["lengths"]), [w["cp"]], w["std"]
+            if args.small:
+                lengths = [32768]  # profiling aid, as in run_long128k
             steps = max(3, min(args.steps, 5))
         T, max_cp = sum(lengths), max(cps_l)
         q, k, v = workloads.qkv_device(T, H, D, args.seed, std=std, device=dev)
@@ -568,7 +571,7 @@ def run_backward(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
         assert cpattn.poll_error(ws) == cpattn.OK
         flops = 2.5 * attention_flops(lengths, H, D)
         tf = flops / (ms * 1e-3) / 1e12
-        sub[name] = {"ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+        sub[name] = {"tokens": T, "ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
                      "frac_of_sustained": tf / bf16_sustained, "flops": flops, "steps": steps}
         del q, k, v, dout, out, lse, ws, dq, dk, dv
         torch.cuda.empty_cache()
