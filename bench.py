@@ -196,6 +196,21 @@ def cpu_oracle_sample(lengths, H, D, seed, budget_s):
     return flops / t_total / 1e12, desc, cores, t_total
 
 
+def main_config(lengths, cp_sizes, H, D, seed):
+    """The `config` of the packed16k line (both arms report it)."""
+    T = sum(lengths)
+    return {
+        "workload": "packed THD micro-batch, 16384-token budget, lognormal(7.5,1) lengths "
+                    "clipped to [64,16384], DPxCP world 4, max_seqlen_per_dp_cp_rank 4096, "
+                    "CP from {1,2,4}, H=32, D=128, causal, bf16 N(0,1)",
+        "lengths": [int(x) for x in lengths], "cp_sizes": [int(x) for x in cp_sizes],
+        "tokens_per_gpu": T, "H": H, "D": D, "seed": seed,
+        "parallelism": "one independent micro-batch per GPU (seed + rank), no collective",
+        "l2": "inputs larger than L2 (Q/K/V %.0f MB per GPU)" % (3 * T * H * D * 2 / 1e6),
+        "step": "cpattn_plan (host) + cp_size upload + cpattn_fwd fused",
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -205,6 +220,8 @@ def run_reference(args, rank, world):
     H, D = w["H"], w["D"]
     import numpy as np
     from oracle import attention as oa
+    from oracle import planner as op
+    plan = op.plan(lengths, w["world"], w["limit"], w["max_cp"])
     # One step = the oracle's full attention on the batch's shortest sample.
     L = min(lengths)
     q, k, v = workloads.qkv(L, H, D, args.seed)
@@ -226,7 +243,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "packed16k sample (CPU oracle)", "sample_len": L, "H": H, "D": D},
+        "config": main_config(lengths, plan["cp_size"], H, D, args.seed),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -466,16 +483,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": "packed THD micro-batch, 16384-token budget, lognormal(7.5,1) lengths "
-                        "clipped to [64,16384], DPxCP world 4, max_seqlen_per_dp_cp_rank 4096, "
-                        "CP from {1,2,4}, H=32, D=128, causal, bf16 N(0,1)",
-            "lengths": lengths, "cp_sizes": [int(x) for x in plan["cp_size"]],
-            "tokens_per_gpu": T, "H": H, "D": D, "seed": args.seed,
-            "parallelism": "one independent micro-batch per GPU (seed + rank), no collective",
-            "l2": "inputs larger than L2 (Q/K/V %.0f MB per GPU)" % (3 * T * H * D * 2 / 1e6),
-            "step": "cpattn_plan (host) + cp_size upload + cpattn_fwd fused",
-        },
+        "config": main_config(lengths, plan["cp_size"], H, D, args.seed),
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,false> + schedule_kernel",
                      "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                      "frac": achieved / bf16_peak, "traffic": traffic,
