@@ -4,7 +4,8 @@ Each case replaces one oracle function with a copy that carries one
 plausible mistake (a dropped scale, a causal off-by-one, a leaking sample
 boundary, swapped operands, a wrong log base, a missing rescale in the merge,
 a floor instead of a ceiling in the chunking, a wrong CP rule, a dropped
-term or transposed operand in the backward), runs the pin
+term or transposed operand in the backward, a wrong weight in the LSE-form
+merge, a strided head grouping, a reordered sample selection), runs the pin
 tests that cover that function, and requires at least one of them to fail.
 The oracle itself is untouched: the copies live in this file and are patched
 in for the duration of one case.  A control case runs the same pins on the
@@ -16,10 +17,16 @@ import pytest
 
 import test_oracle_attention as attn_pins
 import test_oracle_backward as bwd_pins
+import test_oracle_dcp as dcp_pins
+import test_oracle_decode as dec_pins
 import test_oracle_planner as plan_pins
+import test_oracle_ulysses as uly_pins
 from oracle import attention as oa
 from oracle import backward as ob
+from oracle import dcp as od
+from oracle import decode as odc
 from oracle import planner as op
+from oracle import ulysses as ou
 
 
 # ------------------------------------------------------- full attention --
@@ -134,6 +141,50 @@ def _sample_backward_with(mistake):
     return sample_backward
 
 
+# ------------------------------------------- LSE merge, Ulysses, DCP --
+
+def _merge_lse_with(mistake):
+    def merge_lse(o_s, lse_s):
+        o_s = np.asarray(o_s, dtype=np.float64)
+        lse_s = np.asarray(lse_s, dtype=np.float64)
+        mx = lse_s.max(axis=0)
+        ref = np.where(np.isfinite(mx), mx, 0.0)
+        w = np.where(np.isfinite(lse_s), np.exp(lse_s - ref[None]), 0.0)
+        if mistake == "unweighted":
+            w = np.where(np.isfinite(lse_s), 1.0, 0.0)
+        tot = w.sum(axis=0)
+        lse = np.where(tot > 0, ref + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+        if mistake == "lse_is_max":
+            lse = mx
+        o = (w[..., None] * o_s).sum(axis=0)
+        if mistake != "not_renormalised":
+            o = o / np.where(tot > 0, tot, 1.0)[..., None]
+        return o, lse
+
+    return merge_lse
+
+
+def _to_groups_strided(x, P):
+    """Head h to group h mod P (instead of h // (H / P))."""
+    x = np.asarray(x)
+    T, H = x.shape[0], x.shape[1]
+    return np.ascontiguousarray(np.moveaxis(x.reshape((T, H // P, P) + x.shape[2:]), 2, 0))
+
+
+def _from_groups_strided(y, P):
+    y = np.asarray(y)
+    T, Hp = y.shape[1], y.shape[2]
+    return np.ascontiguousarray(np.moveaxis(y, 0, 2).reshape((T, P * Hp) + y.shape[3:]))
+
+
+_ORIG_SELECT = od.select
+
+
+def _select_sorted(x, cu_seqlens, ids):
+    """The samples in index order instead of the order asked for."""
+    return _ORIG_SELECT(x, cu_seqlens, sorted(ids))
+
+
 # ------------------------------------------------------------- planner --
 
 def _cp_size_with(mistake):
@@ -185,6 +236,17 @@ BACKWARD_PINS = [
     bwd_pins.test_length_one_and_constant_values,
     bwd_pins.test_rows_match_the_full_backward,
 ]
+DECODE_PINS = [
+    dec_pins.test_decode_matches_textbook_softmax,
+    dec_pins.test_decode_is_the_last_row_of_causal_attention,
+    dec_pins.test_shards_merge_to_the_whole,
+    dec_pins.test_special_cases,
+]
+ULYSSES_PINS = [uly_pins.test_layout_by_hand_and_round_trip,
+                uly_pins.test_ulysses_attention_equals_full_attention]
+DCP_PINS = [dcp_pins.test_select_layout_and_round_trip,
+            dcp_pins.test_micro_batches_partition_the_batch,
+            dcp_pins.test_dcp_forward_equals_full_attention]
 PLANNER_PINS = [
     plan_pins.test_golden_plans,
     plan_pins.test_page_worked_example_limit,
@@ -217,7 +279,8 @@ def _failures(pins):
 
 
 def test_control_every_pin_passes_on_the_oracle():
-    assert _failures(ATTENTION_PINS + RING_PINS + BACKWARD_PINS + PLANNER_PINS) == 0
+    assert _failures(ATTENTION_PINS + RING_PINS + BACKWARD_PINS + DECODE_PINS + ULYSSES_PINS
+                     + DCP_PINS + PLANNER_PINS) == 0
 
 
 @pytest.mark.parametrize("mistake", ["no_scale", "causal_plus1", "causal_minus1",
@@ -267,3 +330,21 @@ def test_correct_backward_copy_passes_the_pins(monkeypatch):
 def test_backward_mistake_fails_a_pin(monkeypatch, mistake):
     monkeypatch.setattr(ob, "_sample_backward", _sample_backward_with(mistake))
     assert _failures(BACKWARD_PINS) > 0
+
+
+@pytest.mark.parametrize("mistake", ["unweighted", "lse_is_max", "not_renormalised"])
+def test_lse_merge_mistake_fails_a_pin(monkeypatch, mistake):
+    monkeypatch.setattr(odc, "merge_lse", _merge_lse_with(mistake))
+    assert _failures(DECODE_PINS) > 0
+
+
+def test_strided_head_groups_fail_a_pin(monkeypatch):
+    # A consistent pair: round trips still pass, the hand-built layout does not.
+    monkeypatch.setattr(ou, "to_head_groups", _to_groups_strided)
+    monkeypatch.setattr(ou, "from_head_groups", _from_groups_strided)
+    assert _failures(ULYSSES_PINS) > 0
+
+
+def test_reordered_selection_fails_a_pin(monkeypatch):
+    monkeypatch.setattr(od, "select", _select_sorted)
+    assert _failures(DCP_PINS) > 0
