@@ -10,8 +10,36 @@ from long_context_gb300 import workloads
 # Tolerances for bf16 inputs with fp32 accumulation, against the float64 oracle.
 O_ATOL = 2e-2          # attention output, max abs
 LSE_RTOL = 1e-3        # |dLSE| <= 1e-3 * max(1, |LSE|)
-MERGE_ATOL = 1e-5      # fp32 merge output O / l, max abs
+MERGE_RTOL = 1e-5      # fp32 merge output O / l, relative to its row's max |O / l|
 MERGE_L_RTOL = 1e-5    # fp32 merge output l, relative
+
+
+def check_merge_o(got, ref, what=""):
+    """Assert the fp32 merge gate on O / l; returns the largest error relative
+    to its row's max |O / l|.
+
+    A row is one (token, head) vector of D values.  The merge runs in fp32, so
+    every element must agree with the oracle to within MERGE_RTOL of the
+    largest magnitude in its row (fp32 rounding of the fold, a few ulp, is
+    ~1e-7 of it); an O path that went through bf16 anywhere (relative
+    rounding up to 2^-9) misses this by two orders of magnitude.  Rows whose
+    reference is all zero (nothing visible) must be exactly zero."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, what
+    assert np.all(np.isfinite(got)), "%s: non-finite merge output" % what
+    if ref.size == 0:
+        return 0.0
+    d = ref.shape[-1]
+    g2 = got.reshape(-1, d)
+    r2 = ref.reshape(-1, d)
+    row_max = np.max(np.abs(r2), axis=1)
+    zero = row_max == 0
+    assert np.all(g2[zero] == 0), "%s: rows with nothing visible must be zero" % what
+    rel = np.abs(g2[~zero] - r2[~zero]) / row_max[~zero][:, None]
+    worst = float(np.max(rel)) if rel.size else 0.0
+    assert worst <= MERGE_RTOL, "%s: max |dO| / row max |O| = %g" % (what, worst)
+    return worst
 
 
 def check_attention(out, lse, ref_o, ref_lse, what=""):
@@ -84,6 +112,27 @@ def sample_tokens(cu, n_random, seed, extra=()):
                 toks.add(t)
     if T > 0:
         toks.update(int(t) for t in rng.integers(0, T, n_random))
+    return sorted(toks)
+
+
+def chunk_edge_tokens(cu, cps):
+    """Token indices at the ring-chunk edges of every sample with CP > 1: for
+    each boundary between chunk j-1 and chunk j (chunks of ceil(L / c)
+    tokens), the rows around it and one and two 128-row tiles past it."""
+    cu = [int(x) for x in cu]
+    toks = set()
+    for b, c in enumerate(cps):
+        c = int(c)
+        s0, s1 = cu[b], cu[b + 1]
+        L = s1 - s0
+        if c <= 1 or L == 0:
+            continue
+        chunk = -(-L // c)
+        for j in range(1, c + 1):
+            e = min(j * chunk, L)
+            for d in (-129, -128, -1, 0, 1, 127, 128, 255):
+                if 0 <= e + d < L:
+                    toks.add(s0 + e + d)
     return sorted(toks)
 
 

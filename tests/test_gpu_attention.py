@@ -9,8 +9,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import (O_ATOL, check_attention, default_scale, make_batch,
-                     sample_tokens)
+from helpers import (O_ATOL, check_attention, check_merge_o, chunk_edge_tokens,
+                     default_scale, make_batch, sample_tokens)
 from long_context_gb300 import workloads
 from oracle import attention as oa
 from oracle import planner as op
@@ -237,8 +237,13 @@ def test_partials_match_oracle_ring_steps(cp, causal):
     lse_s = m[nz] + np.log(l[nz])
     rlse_s = rm[nz] + np.log(rl[nz])
     assert np.max(np.abs(lse_s - rlse_s) / np.maximum(1, np.abs(rlse_s))) <= 1e-3
-    # Folding them with the library's merge gives the attention result.
+    # Folding them with the library's merge gives the attention result; the
+    # fold itself is fp32 and is held to the fp32 merge gate against the
+    # oracle's fold of the same partials.
     mo, mm, ml = cp.merge(*(torch.from_numpy(x.astype(np.float32)).cuda() for x in (o, m, l)))
+    fo, _, _ = oa.merge_partials(o.astype(np.float32), m.astype(np.float32),
+                                 l.astype(np.float32))
+    check_merge_o(mo.cpu().numpy(), fo, "partials fold")
     ref_o, ref_lse = oa.full_attention(qf, kf, vf, cu, scale, causal=causal)
     check_attention(mo.cpu().numpy(), (mm + torch.log(ml)).cpu().numpy(), ref_o, ref_lse,
                     "partials merged")
@@ -246,22 +251,31 @@ def test_partials_match_oracle_ring_steps(cp, causal):
 
 # ------------------------------------------------------------ full sizes --
 
+# Seed 0 plans every sample at CP 1; seed 1 has two samples at CP 2 (4112
+# and 4471 tokens) and seed 2 one at CP 4 (10935 tokens), so the ring steps
+# run at the full size of the workload too.
+PACKED16K_CPS = {0: [1, 1, 1, 1, 1, 1, 1], 1: [1, 2, 1, 1, 2, 1], 2: [1, 1, 1, 1, 4, 1]}
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_packed16k_workload(cp, mode):
+def test_packed16k_workload(cp, mode, seed):
     """16,384-token packed THD batch at world 4, limit 4096, dynamic CP."""
     w = workloads.WORKLOADS["packed16k"]
-    lengths = workloads.packed_lengths(0, w["budget"])
+    lengths = workloads.packed_lengths(seed, w["budget"])
     plan_c = cp.plan(lengths, w["world"], w["limit"], w["max_cp"])
     plan_o = op.plan(lengths, w["world"], w["limit"], w["max_cp"])
     assert list(plan_c["cp_size"]) == plan_o["cp_size"]
     cps = [int(x) for x in plan_c["cp_size"]]
+    assert cps == PACKED16K_CPS[seed]
     H, D = w["H"], w["D"]
-    (q, k, v, cu), g = make_batch(lengths, H, D, seed=0)
+    (q, k, v, cu), g = make_batch(lengths, H, D, seed=seed)
     scale = default_scale(D)
     out, lse = _run(cp, g, lengths, cps, H, D, True, mode, scale)
-    toks = sample_tokens(cu, 48, seed=0)
+    toks = sample_tokens(cu, 48, seed=seed, extra=chunk_edge_tokens(cu, cps))
     ref_o, ref_lse = oa.attention_rows(q, k, v, cu, scale, toks)
-    check_attention(out[toks], lse[toks], ref_o, ref_lse, "packed16k mode %d" % mode)
+    check_attention(out[toks], lse[toks], ref_o, ref_lse,
+                    "packed16k seed %d mode %d" % (seed, mode))
 
 
 @pytest.mark.parametrize("mode", [0, 1])
@@ -291,24 +305,40 @@ def test_sweep256_workload(cp):
     H, D = w["H"], w["D"]
     scale = default_scale(D)
     rng = np.random.default_rng(0)
-    checked = 0
-    for mb in range(plan_c["num_micro_batches"]):
+    n_mb = plan_c["num_micro_batches"]
+    rows = 0
+    for mb in range(n_mb):
         members = [b for b in range(len(lengths)) if plan_c["micro_batch"][b] == mb]
         lens = [lengths[b] for b in members]
         cps = [int(plan_c["cp_size"][b]) for b in members]
         # Each micro-batch draws its own tensors on the GPU (seed = 1000 + id);
-        # the oracle reads back only the samples it checks.
+        # the oracle reads back only the rows it checks.
         q, k, v = workloads.qkv_device(sum(lens), H, D, seed=1000 + mb)
         cu = workloads.cu_seqlens(lens)
         cu_t = torch.from_numpy(cu).cuda()
         cps_t = torch.tensor(cps, dtype=torch.int32, device="cuda")
         out, lse = cp.fwd(q, k, v, cu_t, cps_t, max_seqlen=max(lens),
                           max_cp=w["max_cp"], softmax_scale=scale)
-        if mb % 8 == 0 or mb == plan_c["num_micro_batches"] - 1:
-            toks = sorted(set(int(t) for t in rng.integers(0, int(cu[-1]), 6)) |
-                          {int(cu[-1]) - 1, int(cu[1]) - 1})
-            ref_o, ref_lse = oa.attention_rows(q, k, v, cu, scale, toks)
-            check_attention(out[toks].float().cpu().numpy(), lse[toks].cpu().numpy(),
-                            ref_o, ref_lse, "sweep256 mb %d" % mb)
-            checked += 1
-    assert checked >= 2
+        # Every micro-batch: the first and last row of each sample, the rows
+        # around one chunk edge of each CP > 1 sample, and random rows, at
+        # least 16 in all.
+        edge = {}
+        for b in range(len(lens)):
+            s0, s1 = int(cu[b]), int(cu[b + 1])
+            edge[s0] = edge[s1 - 1] = True
+            if cps[b] > 1:
+                chunk = -(-lens[b] // cps[b])
+                j = int(rng.integers(1, cps[b]))
+                for d in (-1, 0, 128):
+                    t = s0 + min(j * chunk, lens[b]) + d
+                    if s0 <= t < s1:
+                        edge[t] = True
+        toks = set(edge) | set(int(t) for t in rng.integers(0, int(cu[-1]), 8))
+        while len(toks) < 16:
+            toks.add(int(rng.integers(0, int(cu[-1]))))
+        toks = sorted(toks)
+        ref_o, ref_lse = oa.attention_rows(q, k, v, cu, scale, toks)
+        check_attention(out[toks].float().cpu().numpy(), lse[toks].cpu().numpy(),
+                        ref_o, ref_lse, "sweep256 mb %d" % mb)
+        rows += len(toks)
+    assert rows >= 16 * n_mb

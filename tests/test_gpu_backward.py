@@ -2,9 +2,10 @@
 
 The GPU backward takes the GPU forward's O and LSE (the product path: forward
 then backward); the oracle computes everything from Q, K, V and dO alone.
-Small cases compare every element; the full-size packed batch compares
-sampled dQ rows (computed one by one) and the identities that hold at any
-size: per sample and head, sum_j dV_j = sum_i dO_i and sum_j dK_j = 0.
+Small cases and the full-size packed 16K batch compare every element; the
+131,072-token sequence compares sampled dQ rows (computed one by one) and the
+identities that hold at any size: per sample and head, sum_j dV_j = sum_i dO_i
+and sum_j dK_j = 0.
 """
 
 import numpy as np
@@ -112,24 +113,28 @@ def test_backward_empty_batch(cp):
     assert cp.poll_error(ws) == cp.OK and dq.numel() == 0
 
 
-def test_backward_packed16k_rows_and_identities(cp):
-    """The packed 16K batch (7 samples, H=32, D=128, CP 1/2/4 from the plan):
-    sampled dQ rows against the oracle, and per (sample, head)
-    sum_j dV_j = sum_i dO_i, sum_j dK_j = 0 -- each checked relative to the
-    size of the summed terms."""
+@pytest.mark.parametrize("seed,heads", [(0, None), (1, (0, 13, 31))])
+def test_backward_packed16k_every_element(cp, seed, heads):
+    """The packed 16K batch (H=32, D=128, CP from the plan: all 1 for seed 0,
+    two samples at CP 2 for seed 1) at full size: every element of dQ, dK and
+    dV against the oracle's full backward, taken one head at a time (the
+    oracle holds L^2 scores per head; every head for seed 0, three for seed 1,
+    whose heads differ only in their data), and per (sample, head)
+    sum_j dV_j = sum_i dO_i, sum_j dK_j = 0."""
     w = workloads.WORKLOADS["packed16k"]
     H, D = w["H"], w["D"]
-    lengths = workloads.packed_lengths(0, w["budget"])
+    lengths = workloads.packed_lengths(seed, w["budget"])
     plan = cp.plan(lengths, w["world"], w["limit"], w["max_cp"])
     cps = [int(c) for c in plan["cp_size"]]
-    q, k, v, do, cu = _inputs(lengths, H, D, seed=0)
+    q, k, v, do, cu = _inputs(lengths, H, D, seed=seed)
     scale = default_scale(D)
     dq, dk, dv = _fwd_bwd(cp, q, k, v, do, cu, cps, True, scale)
-    toks = [int(t) for t in np.random.default_rng(5).integers(0, int(cu[-1]), 40)]
-    toks += [int(c) for c in cu[:-1]] + [int(c) - 1 for c in cu[1:]]
-    ref_dq, _, _ = ob.backward_rows(q, k, v, do, cu, scale, toks)
-    check_grad(dq[toks], ref_dq, "dq rows")
-    dof = do.float().numpy().astype(np.float64)
+    qf, kf, vf, dof = (workloads.to_f64(x) for x in (q, k, v, do))
+    for h in (range(H) if heads is None else heads):
+        sl = slice(h, h + 1)
+        ref = ob.full_attention_backward(qf[:, sl], kf[:, sl], vf[:, sl], dof[:, sl], cu, scale)
+        for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+            check_grad(got[:, sl], ref[name], "seed %d head %d %s" % (seed, h, name))
     for b in range(len(lengths)):
         s0, s1 = int(cu[b]), int(cu[b + 1])
         sum_dv = dv[s0:s1].astype(np.float64).sum(0)

@@ -1,10 +1,14 @@
-"""GPU parity of cpattn_merge against the oracle's step-by-step fold."""
+"""GPU parity of cpattn_merge against the oracle's step-by-step fold.
+
+The merge is fp32 throughout, so O / l is held to MERGE_RTOL relative to its
+row's largest magnitude (helpers.check_merge_o), l to MERGE_L_RTOL relative,
+and m exactly up to fp32 rounding of the maximum."""
 
 import numpy as np
 import pytest
 import torch
 
-from helpers import MERGE_ATOL, MERGE_L_RTOL
+from helpers import MERGE_L_RTOL, check_merge_o
 from long_context_gb300 import workloads
 from oracle import attention as oa
 
@@ -33,7 +37,8 @@ def _check(cp, o, m, l, rows=None):
         ro, rm, rl = oa.merge_partials(o[:, t_idx, h_idx].numpy(), m[:, t_idx, h_idx].numpy(),
                                        l[:, t_idx, h_idx].numpy())
         go_, gm_, gl_ = go[t_idx, h_idx], gm[t_idx, h_idx], gl[t_idx, h_idx]
-    assert np.max(np.abs(go_ - ro)) <= MERGE_ATOL
+    worst = check_merge_o(go_, ro, "merge S=%d T=%d H=%d D=%d" % (S, T, H, D))
+    print("merge S=%d T=%d H=%d D=%d: max |dO| / row max |O| = %.3g" % (S, T, H, D, worst))
     fin = np.isfinite(rm)
     assert np.array_equal(np.isfinite(gm_), fin)
     assert np.max(np.abs(gm_[fin] - rm[fin]), initial=0) <= 1e-6
