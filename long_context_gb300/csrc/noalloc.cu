@@ -12,10 +12,14 @@
 // The scratch is a file-scope __device__ array of kNoAllocScratchBytes; every
 // GPU that loads the library holds it until the process exits.  Host code
 // cannot pass the array's name to a kernel (on the host that name is only a
-// stand-in for the device symbol), so the first call on each device, with
-// that device current, looks up its device address with cudaGetSymbolAddress
-// and caches it.  Nothing here calls cudaMalloc, cudaFree or any allocating
-// library routine.
+// stand-in for the device symbol), so the first call in each CUDA context
+// (normally one per device: the primary context), with that device current,
+// looks up its device address with cudaGetSymbolAddress and caches it under
+// the context.  A context created later -- for example after
+// cudaDeviceReset, which loads the module anew and may place the array
+// elsewhere -- gets its own lookup.  Nothing here calls cudaMalloc, cudaFree
+// or any allocating library routine.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,8 +29,16 @@
 #include "cpattn.h"
 #include "kernels.h"
 
-// Size of the fixed scratch: enough for the work list of any problem with
-// T / 256 + B * max_cp below about 130,000 (for example a 16M-token batch).
+// Size of the fixed scratch.  It must hold the fused forward's workspace
+// (ws_layout in api.cu): a 256-byte header, 4 (B + 1) bytes of per-sample
+// prefix, and 8 + 16 H bytes per work item, each part rounded up to 256 bytes,
+// with n_items = T / 256 + B * max_cp + 1.  So a problem fits when
+//   256 + 4 (B + 1) + (8 + 16 H) n_items  (+ up to 768 bytes of rounding)
+// stays within 1 MiB.  At H = 32 that is about 2,000 work items: for example
+// a 16,384-token batch of 7 samples at max_cp 4 needs 93 items (49 KB), and
+// the largest micro-batch of the 256-sample sweep (max_cp 8) 154 items
+// (81 KB); one call over the whole sweep (4.4 M tokens) or over about 510K
+// tokens at H = 32 is refused.  At H = 1 the limit is about 43,000 items.
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -35,23 +47,42 @@ namespace cpattn {
 
 namespace {
 
-std::mutex g_scratch_mu;
-std::unordered_map<int, void*> g_scratch_ptr;  // device ordinal -> address
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
-// Device address of g_noalloc_scratch on the current device (set up once per
-// device).
+std::mutex g_scratch_mu;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+std::unordered_map<CUcontext, void*> g_scratch_ptr;  // CUDA context -> address
+
+// Device address of g_noalloc_scratch in the current device's context (looked
+// up once per context).
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CPATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  auto it = g_scratch_ptr.find(dev);
-  if (it == g_scratch_ptr.end()) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+  if (g_ctx_get_current == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
       return CPATTN_ERR_CUDA;
-    it = g_scratch_ptr.emplace(dev, ptr).first;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
   }
-  *out = it->second;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return CPATTN_ERR_CUDA;
+  if (ctx != nullptr) {
+    auto it = g_scratch_ptr.find(ctx);
+    if (it != g_scratch_ptr.end()) {
+      *out = it->second;
+      return CPATTN_OK;
+    }
+  }
+  // Set-up for this context: the runtime makes the current device's primary
+  // context current here if this thread had none yet.
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+    return CPATTN_ERR_CUDA;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CPATTN_ERR_CUDA;
+  g_scratch_ptr[ctx] = ptr;
+  *out = ptr;
   return CPATTN_OK;
 }
 
