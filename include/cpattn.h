@@ -59,7 +59,9 @@ typedef enum {
   CPATTN_ERR_WORKSPACE_TOO_SMALL = 3,
   CPATTN_ERR_PLAN_INFEASIBLE = 4,    /* a sample does not fit at max_cp          */
   CPATTN_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed        */
-  CPATTN_ERR_DEVICE_TIMEOUT = 6      /* a kernel's bounded wait ran out          */
+  CPATTN_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out          */
+  CPATTN_ERR_DEVICE_BOUNDS = 7       /* debug build only: a kernel's bounds check
+                                        failed (the access was skipped)          */
 } cpattn_status;
 
 /* Kernel modes of cpattn_fwd. */
@@ -395,9 +397,16 @@ int cpattn_ulysses_seqlens(const int32_t* cu_seqlens, const int32_t* cp_size,
  * Limits and behaviour:
  *   - Problems whose fused workspace (cpattn_fwd_workspace_size(T, B, H, D,
  *     max_cp, CPATTN_MODE_FUSED)) exceeds 1 MiB are rejected with
- *     CPATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *   - The first call on each device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture.
+ *     CPATTN_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  That size
+ *     is about 256 + 4 (B + 1) + (8 + 16 H) (T / 256 + B max_cp + 1) bytes
+ *     (each of the three parts rounded up to 256): at H = 32 some 2,000 work
+ *     items, e.g. a 16,384-token batch of 7 samples at max_cp 4 uses 49 KB,
+ *     while one call over more than about 510K tokens is refused.
+ *   - The first call in each CUDA context (normally the device's primary
+ *     context; with that device current) looks up the array's device address
+ *     and caches it for that context; make that first call before any stream
+ *     capture.  A context created later (e.g. after cudaDeviceReset) gets its
+ *     own lookup on its first call.
  *   - Every call shares the one array and leaves its contents behind; each
  *     call clears the parts that must start at zero itself.  Calls whose
  *     kernels overlap on the GPU (for example on two streams at once) race on

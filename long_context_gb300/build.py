@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libcpattn.so")
 
 SOURCES = ["plan.cpp", "api.cu", "schedule.cu", "merge.cu", "attn_fwd.cu", "attn_bwd.cu",
            "dcp.cu", "decode.cu", "noalloc.cu", "ulysses.cu"]
-HEADERS = ["kernels.h", "ptx.cuh", "work.cuh"]
+HEADERS = ["kernels.h", "ptx.cuh", "work.cuh", "debug.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -53,21 +53,17 @@ def _stale():
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_fault_injection(force=False):
-    """Test-only variant ``libcpattn_fault.so`` built with
-    ``-DCPATTN_FAULT_INJECT_DROP_P``: the attention kernel's first CTA skips
-    one hand-off so that a bounded device wait runs out.  Used by the failure
-    detection test; never loaded by the package."""
-    lib = os.path.join(PKG, "libcpattn_fault.so")
+def _build_variant(name, define, force):
+    lib = os.path.join(PKG, "lib%s.so" % name)
     build()
     if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(LIB):
         return lib
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    flags = _flags() + ["-DCPATTN_FAULT_INJECT_DROP_P=1"]
+    flags = _flags() + ["-D%s=1" % define]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, "fault_" + src + ".o")
+        obj = os.path.join(BUILD, name + "_" + src + ".o")
         r = subprocess.run([nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj],
                            capture_output=True, text=True)
         if r.returncode != 0:
@@ -83,6 +79,23 @@ def build_fault_injection(force=False):
         raise RuntimeError("link failed:\n%s" % r.stderr)
     os.replace(tmp, lib)
     return lib
+
+
+def build_fault_injection(force=False):
+    """Test-only variant ``libcpattn_fault.so`` built with
+    ``-DCPATTN_FAULT_INJECT_DROP_P``: the attention kernel's first CTA skips
+    one hand-off so that a bounded device wait runs out.  Used by the failure
+    detection test; never loaded by the package."""
+    return _build_variant("cpattn_fault", "CPATTN_FAULT_INJECT_DROP_P", force)
+
+
+def build_debug(force=False):
+    """Debug variant ``libcpattn_debug.so`` built with ``-DCPATTN_DEBUG``: the
+    attention kernels (forward, backward, schedule) check every global index
+    and TMA coordinate they derive and report a violation as
+    CPATTN_ERR_DEVICE_BOUNDS in the workspace error word (never a trap).
+    Same C ABI as libcpattn.so."""
+    return _build_variant("cpattn_debug", "CPATTN_DEBUG", force)
 
 
 def build(force=False, verbose_ptxas=False, quiet=True):

@@ -422,6 +422,7 @@ extern "C" int cpattn_bwd(const void* q, const void* k, const void* v, const voi
   bp.scale = softmax_scale;
   bp.scale_log2 = softmax_scale * 1.4426950408889634f;
   bp.hdr = hdr;
+  bp.total_tokens = total_tokens;
   bp.table = sp.table_asc;
   if (launch_bwd_dkdv(tq, tk, tv, tdo, bp, head_dim, grid, s) != cudaSuccess)
     return CPATTN_ERR_CUDA;
@@ -552,6 +553,7 @@ extern "C" const char* cpattn_status_string(int status) {
     case CPATTN_ERR_PLAN_INFEASIBLE: return "plan infeasible";
     case CPATTN_ERR_CUDA: return "CUDA error";
     case CPATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case CPATTN_ERR_DEVICE_BOUNDS: return "device bounds check failed (debug build)";
     default: return "unknown status";
   }
 }

@@ -43,6 +43,7 @@
 //   dV += P^T dO, dK += dS^T Q.
 #include <cuda_bf16.h>
 
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "work.cuh"
@@ -233,13 +234,26 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b, u
            (acc || kk > 0) ? 1u : 0u);
 }
 
-// Loads a 128-row bf16 tile (rows row0.., head h) into shared memory.
+// Loads a 128-row bf16 tile (rows row0.., head h) into shared memory.  (The
+// debug build checks row0 against the T rows of the tensor.)
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                          int h, int row0, uint64_t pol) {
+                                          int h, int row0, uint64_t pol, const BwdParams& p) {
+  row0 = checked_coord(row0, 0, static_cast<int>(p.total_tokens), p.hdr);
 #pragma unroll
   for (int hf = 0; hf < D / 64; ++hf)
     tma_load_3d(dst + hf * 16384, map, bar, hf * 64, h, row0, pol);
+}
+
+// The debug build's check of a work entry: rows of this batch, a valid head,
+// CP size, rank and block start (false: the CTA does nothing).
+__device__ __forceinline__ bool unit_in_bounds(int tok0, int L, int h, int c, int rank,
+                                               int first, int chunk_end, const BwdParams& p) {
+  if (!kDebugChecks) return true;
+  return in_bounds(tok0, 0, p.total_tokens + 1, p.hdr) &&
+         in_bounds(static_cast<long long>(tok0) + L, 0, p.total_tokens + 1, p.hdr) &&
+         in_bounds(h, 0, p.num_heads, p.hdr) && in_bounds(c, 1, kMaxCp + 1, p.hdr) &&
+         in_bounds(rank, 0, c, p.hdr) && in_bounds(first, 0, chunk_end, p.hdr);
 }
 
 // Byte offset of 16-byte chunk c of row r in a 128-row tile buffer laid out
@@ -377,6 +391,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kv0 = min(u.rank * u.chunk, u.L) + u.blk * kT;        // first key of the tile
   const int kv_blk_end = min(kv0 + kT, min((u.rank + 1) * u.chunk, u.L));
   KRing ring{u.L, u.c, u.chunk, u.rank, p.causal, kv0};
+  if (!unit_in_bounds(u.tok0, u.L, u.h, u.c, u.rank, kv0, min((u.rank + 1) * u.chunk, u.L), p))
+    return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -421,16 +437,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
-    load_tile<D>(smem + C::kA0Off, &tm_k, a_full, u.h, u.tok0 + kv0, pol_kv);
-    load_tile<D>(smem + C::kA1Off, &tm_v, a_full, u.h, u.tok0 + kv0, pol_kv);
+    load_tile<D>(smem + C::kA0Off, &tm_k, a_full, u.h, u.tok0 + kv0, pol_kv, p);
+    load_tile<D>(smem + C::kA1Off, &tm_v, a_full, u.h, u.tok0 + kv0, pol_kv, p);
     Walk<KRing> w;
     w.start(ring);
     if (!w.done(ring)) {  // query tile 0 goes to stage 0, which is free
       const int row = u.tok0 + w.tile_row();
       mbar_arrive_expect_tx(&b0_full[0], C::kTileBytes);
-      load_tile<D>(smem + C::kB0Off, &tm_q, &b0_full[0], u.h, row, pol_q);
+      load_tile<D>(smem + C::kB0Off, &tm_q, &b0_full[0], u.h, row, pol_q, p);
       mbar_arrive_expect_tx(&b1_full[0], C::kTileBytes);
-      load_tile<D>(smem + C::kB1Off, &tm_do, &b1_full[0], u.h, row, pol_q);
+      load_tile<D>(smem + C::kB1Off, &tm_do, &b1_full[0], u.h, row, pol_q, p);
     }
   }
   if (warp == 9) {
@@ -472,12 +488,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = wait_bounded(&b0_empty[st0], ph0 ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&b0_full[st0], C::kTileBytes);
-          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_q, &b0_full[st0], u.h, row, pol_q);
+          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_q, &b0_full[st0], u.h, row, pol_q, p);
           ++nb0;
           ok = wait_bounded(&b1_empty[st1], ph1 ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&b1_full[st1], C::kTileBytes);
-          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_do, &b1_full[st1], u.h, row, pol_q);
+          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_do, &b1_full[st1], u.h, row, pol_q, p);
           ++nb1;
         }
         if (!ok) {
@@ -614,7 +630,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // warps 0-3 load its LSE, warps 4-7 its D.
         const int qp = qt0 + r;
         float val = ch == 0 ? kInf : 0.f;  // +inf LSE: P = 0 outside the chunk
-        if (qp < w.end) {
+        if (qp < w.end && in_bounds(u.tok0 + qp, 0, p.total_tokens, p.hdr)) {
           const size_t ri = static_cast<size_t>(u.tok0 + qp) * p.num_heads + u.h;
           val = ch == 0 ? __ldg(&p.lse[ri]) * kLog2e : __ldg(&p.delta[ri]);
         }
@@ -718,7 +734,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // MMA reading them has completed).
         const size_t ri0 = static_cast<size_t>(u.tok0 + kv0) * p.num_heads + u.h;
         const size_t ld = static_cast<size_t>(p.num_heads) * D;
-        const int n_rows = kv_blk_end - kv0;
+        const int n_rows =
+            in_bounds(static_cast<long long>(u.tok0) + kv_blk_end, 1, p.total_tokens + 1, p.hdr)
+                ? kv_blk_end - kv0
+                : 0;
         if (ch == 0)
           store_rows_staged<D>(row_addr + 2 * kT, 1.f, smem + C::kA0Off, r, 0, lane,
                                (warp & 3) * 32, p.dv + ri0 * D, ld, n_rows);
@@ -766,6 +785,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int q0 = min(u.rank * u.chunk, u.L) + u.blk * kT;
   const int q_blk_end = min(q0 + kT, min((u.rank + 1) * u.chunk, u.L));
   QRing ring{u.L, u.c, u.chunk, u.rank, p.causal, q_blk_end};
+  if (!unit_in_bounds(u.tok0, u.L, u.h, u.c, u.rank, q0, min((u.rank + 1) * u.chunk, u.L), p)) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -809,16 +832,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
-    load_tile<D>(smem + C::kA0Off, &tm_q, a_full, u.h, u.tok0 + q0, pol_q);
-    load_tile<D>(smem + C::kA1Off, &tm_do, a_full, u.h, u.tok0 + q0, pol_q);
+    load_tile<D>(smem + C::kA0Off, &tm_q, a_full, u.h, u.tok0 + q0, pol_q, p);
+    load_tile<D>(smem + C::kA1Off, &tm_do, a_full, u.h, u.tok0 + q0, pol_q, p);
     Walk<QRing> w;
     w.start(ring);
     if (!w.done(ring)) {
       const int row = u.tok0 + w.tile_row();
       mbar_arrive_expect_tx(&b0_full[0], C::kTileBytes);
-      load_tile<D>(smem + C::kB0Off, &tm_k, &b0_full[0], u.h, row, pol_kv);
+      load_tile<D>(smem + C::kB0Off, &tm_k, &b0_full[0], u.h, row, pol_kv, p);
       mbar_arrive_expect_tx(&b1_full[0], C::kTileBytes);
-      load_tile<D>(smem + C::kB1Off, &tm_v, &b1_full[0], u.h, row, pol_kv);
+      load_tile<D>(smem + C::kB1Off, &tm_v, &b1_full[0], u.h, row, pol_kv, p);
     }
   }
   if (warp == 9) {
@@ -860,12 +883,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = wait_bounded(&b0_empty[st0], ph0 ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&b0_full[st0], C::kTileBytes);
-          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_k, &b0_full[st0], u.h, row, pol_kv);
+          load_tile<D>(smem + C::kB0Off + st0 * C::kTileBytes, &tm_k, &b0_full[st0], u.h, row, pol_kv, p);
           ++nb0;
           ok = wait_bounded(&b1_empty[st1], ph1 ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&b1_full[st1], C::kTileBytes);
-          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_v, &b1_full[st1], u.h, row, pol_kv);
+          load_tile<D>(smem + C::kB1Off + st1 * C::kTileBytes, &tm_v, &b1_full[st1], u.h, row, pol_kv, p);
           ++nb1;
         }
         if (!ok) {
@@ -982,7 +1005,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t row_addr = tmem + lane_base;
     const int q_pos = q0 + r;
-    const bool row_valid = q_pos < q_blk_end;
+    const bool row_valid =
+        q_pos < q_blk_end && in_bounds(u.tok0 + q_pos, 0, p.total_tokens, p.hdr);
     const size_t ri = static_cast<size_t>(u.tok0 + q_pos) * p.num_heads + u.h;
     const float lse2 = row_valid ? __ldg(&p.lse[ri]) * kLog2e : 0.f;
     const float dlt = row_valid ? __ldg(&p.delta[ri]) : 0.f;
@@ -1065,7 +1089,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const size_t ri0 = static_cast<size_t>(u.tok0 + q0) * p.num_heads + u.h;
         store_rows_staged<D / 2>(row_addr + 2 * kT + ch * (D / 2), p.scale, smem + C::kA0Off, r,
                                  ch * (D / 2), lane, (warp & 3) * 32, p.dq + ri0 * D,
-                                 static_cast<size_t>(p.num_heads) * D, q_blk_end - q0);
+                                 static_cast<size_t>(p.num_heads) * D,
+                                 in_bounds(static_cast<long long>(u.tok0) + q_blk_end, 1,
+                                           p.total_tokens + 1, p.hdr)
+                                     ? q_blk_end - q0
+                                     : 0);
         tc_fence_before();
       }
     }

@@ -33,6 +33,7 @@
 // next S_t is issued after PV_t, and tcgen05 MMAs of one thread run in order.
 #include <cuda_bf16.h>
 
+#include "debug.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "work.cuh"
@@ -189,6 +190,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   ring.q_blk_end = min(q0 + kRowsPerItem, qc_hi);
   // The second Q tile is skipped when the block has no rows for it.
   const int nq = (q0 + kBM < ring.q_blk_end) ? kNQ : 1;
+  if (kDebugChecks) {
+    // The work entry must address rows of this batch and a valid head, CP
+    // size, rank and block (every CTA thread reads the same entry, so the
+    // whole CTA leaves together, before any barrier or TMEM allocation).
+    const bool ok = in_bounds(tok0, 0, p.total_tokens + 1, p.hdr) &&
+                    in_bounds(static_cast<long long>(tok0) + geo.L, 0, p.total_tokens + 1,
+                              p.hdr) &&
+                    in_bounds(h, 0, p.num_heads, p.hdr) &&
+                    in_bounds(geo.c, 1, kMaxCp + 1, p.hdr) &&
+                    in_bounds(rank, 0, geo.c, p.hdr) && in_bounds(q0, 0, qc_hi, p.hdr);
+    if (!ok) return;
+  }
+  const int T32 = static_cast<int>(p.total_tokens);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -236,14 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
-    for (int t = 0; t < nq; ++t)
+    for (int t = 0; t < nq; ++t) {
+      const int qrow = checked_coord(tok0 + q0 + t * kBM, 0, T32, p.hdr);
       for (int hf = 0; hf < C::kHalves; ++hf)
         tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
-                    hf * 64, h, tok0 + q0 + t * kBM, pol_q);
+                    hf * 64, h, qrow, pol_q);
+    }
     Cursor cur;
     cur.start(ring);
     if (cur.s < ring.num_steps) {  // tile 0 goes to stage 0, which is free
-      const int row = tok0 + cur.kv_lo;
+      const int row = checked_coord(tok0 + cur.kv_lo, 0, T32, p.hdr);
       mbar_arrive_expect_tx(&k_full[0], C::kTileBytes);
       for (int hf = 0; hf < C::kHalves; ++hf)
         tma_load_3d(smem + C::kKOff + hf * 16384, &tm_k, &k_full[0], hf * 64, h, row,
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int x = nk;
           const int st = x % C::kStages;
           const uint32_t ph = (x / C::kStages) & 1;
-          const int row = tok0 + cur.kv_lo + cur.kt * kBN;
+          const int row = checked_coord(tok0 + cur.kv_lo + cur.kt * kBN, 0, T32, p.hdr);
           ok = wait_bounded(&k_empty[st], ph ^ 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
@@ -486,7 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring.seg(s, kv_lo, nt, kv_end);
         if (PARTIALS) {
           if (nt == 0) {
-            if (row_valid) {
+            if (row_valid &&
+                in_bounds(static_cast<long long>(row_idx), 0, p.total_tokens * p.num_heads,
+                          p.hdr)) {
               const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
               float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
               for (int q = 0; q < D / 4; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -608,13 +626,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const size_t so = static_cast<size_t>(s) * p.total_tokens * p.num_heads + row_idx;
           float4* dst = reinterpret_cast<float4*>(p.o_steps + so * D);
+          const bool row_store =
+              row_valid && in_bounds(static_cast<long long>(row_idx), 0,
+                                     p.total_tokens * p.num_heads, p.hdr);
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t orr[32];
             tmem_ld32(o_addr + q * 32, orr);
             tmem_wait_ld();
             reg_fence32(orr);
-            if (row_valid) {
+            if (row_store) {
 #pragma unroll
               for (int e = 0; e < 32; e += 4)
                 dst[q * 8 + e / 4] =
@@ -622,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __uint_as_float(orr[e + 2]), __uint_as_float(orr[e + 3]));
             }
           }
-          if (row_valid) {
+          if (row_store) {
             p.m_steps[so] = (m_run == kNegInf) ? kNegInf : m_run * kLn2;
             p.l_steps[so] = l_run;
           }
@@ -675,9 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&staged[t]);
             if ((warp & 3) == 0 && lane == 0) {
               if (wait_bounded(&staged[t], 0, abort_flag)) {
+                const int orow = tok0 + q0 + t * kBM;
+                if (in_bounds(orow, 0, p.total_tokens - kBM + 1, p.hdr)) {
 #pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf)
-                  tma_store_3d(&tm_o, stage + hf * 16384, hf * 64, h, tok0 + q0 + t * kBM);
+                  for (int hf = 0; hf < C::kHalves; ++hf)
+                    tma_store_3d(&tm_o, stage + hf * 16384, hf * 64, h, orow);
+                }
                 bulk_commit_group();
                 bulk_wait_group_read0();
               } else {
@@ -700,12 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rr = row_w + it * kRpi + lane / kLpr;
               const uint4 val = *reinterpret_cast<const uint4*>(stage + swizzle128(rr, c));
               const int qp = q0 + t * kBM + rr;
-              if (qp < ring.q_blk_end)
+              if (qp < ring.q_blk_end && in_bounds(tok0 + qp, 0, p.total_tokens, p.hdr))
                 *reinterpret_cast<uint4*>(
                     p.out + (static_cast<size_t>(tok0 + qp) * p.num_heads + h) * D + c * 8) = val;
             }
           }
-          if (row_valid && p.lse != nullptr)
+          if (row_valid && p.lse != nullptr &&
+              in_bounds(static_cast<long long>(row_idx), 0, p.total_tokens * p.num_heads,
+                        p.hdr))
             p.lse[row_idx] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : kNegInf;
           tc_fence_before();
         }

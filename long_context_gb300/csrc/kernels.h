@@ -101,6 +101,7 @@ struct BwdParams {
   float scale;       // softmax scale (applied to dQ and dK at the end)
   float scale_log2;  // softmax scale * log2(e)
   WsHeader* hdr;
+  long long total_tokens;  // T (bounds of the debug build's checks)
 };
 
 struct MergeParams {

@@ -9,6 +9,7 @@
 // in it the first CTA index of that sample, and then the work of every CTA
 // (sample start and length, CP size, head, rank, block) into a table that the
 // attention kernel reads with one load per CTA.
+#include "debug.cuh"
 #include "kernels.h"
 #include "work.cuh"
 
@@ -104,8 +105,10 @@ __global__ void __launch_bounds__(kSchedThreads)
     }
   }
   __syncthreads();
-  for (int b = tid; b < p.num_seqs; b += kSchedThreads)
-    p.order[atomicAdd(&hist[bucket(b)], 1)] = b;
+  for (int b = tid; b < p.num_seqs; b += kSchedThreads) {
+    const int slot = atomicAdd(&hist[bucket(b)], 1);
+    if (in_bounds(slot, 0, p.num_seqs, p.hdr)) p.order[slot] = b;
+  }
   __syncthreads();
 
   // First CTA of each sample position: prefix of items * heads.
@@ -167,6 +170,9 @@ __global__ void __launch_bounds__(kSchedThreads)
       int rank, blk;
       item_coords(g, n_b - 1 - local, rank, blk, rows);
       const int tok0 = p.cu_seqlens[b];
+      if (!in_bounds(x, 0, p.max_ctas, p.hdr) || !in_bounds(b, 0, p.num_seqs, p.hdr) ||
+          !in_bounds(h, 0, p.num_heads, p.hdr))
+        continue;
       p.table[x] = make_int4(tok0, g.L, (h << 8) | g.c,
                              static_cast<int>((static_cast<unsigned>(blk) << 8) |
                                               static_cast<unsigned>(rank)));
