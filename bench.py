@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the 128K, unfused and merge sub-measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="NVTX ranges around the library calls and each measurement "
+                         "(for profilers that filter by range)")
     ap.add_argument("--small", action="store_true",
                     help="profiling aid: the long-sequence forward and backward (one "
                          "32768-token sequence), dcp, decode and ulysses measurements on "
@@ -55,7 +58,7 @@ def parse_args():
                          "configuration")
     ap.add_argument("--only", default=None,
                     choices=[None, "main", "long128k", "merge8", "backward", "dcp", "decode",
-                             "ulysses", "sweep256"],
+                             "ulysses", "sweep256", "seeds", "dcp_sweep256"],
                     help="run one measurement only (for profiling)")
     return ap.parse_args()
 
@@ -272,6 +275,7 @@ def time_loop(torch, fn, steps, warmup, stream):
 def main():
     args = parse_args()
     rank, world, local = dist_setup(args)
+    args.rank = rank
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
@@ -282,6 +286,8 @@ def main():
     from long_context_gb300 import build as lib_build
     lib_build.build()
     from long_context_gb300 import cpattn, workloads
+    if args.nvtx:
+        cpattn.set_tracing(True)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -320,10 +326,12 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if args.only in ("long128k", "merge8", "backward", "dcp", "decode", "ulysses", "sweep256"):
+    if args.only in ("long128k", "merge8", "backward", "dcp", "decode", "ulysses", "sweep256",
+                     "seeds", "dcp_sweep256"):
         fn = {"long128k": run_long128k, "merge8": run_merge8, "backward": run_backward,
               "dcp": run_dcp_permute, "decode": run_decode, "ulysses": run_ulysses,
-              "sweep256": run_sweep256}[args.only]
+              "sweep256": run_sweep256, "seeds": run_packed16k_seeds,
+              "dcp_sweep256": run_dcp_sweep256}[args.only]
         res = fn(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak)
         clk = clocks.stop()
@@ -452,10 +460,14 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        for fn in (run_long128k, run_merge8, run_backward, run_dcp_permute, run_decode,
-                   run_ulysses, run_sweep256):
+        for fn in (run_packed16k_seeds, run_long128k, run_merge8, run_backward,
+                   run_dcp_permute, run_decode, run_ulysses, run_sweep256, run_dcp_sweep256):
+            if args.nvtx:
+                torch.cuda.nvtx.range_push("bench:" + fn.__name__[4:])
             extras.update(fn(torch, cpattn, workloads, dev, stream, args, clocks,
                              bf16_peak, bf16_sustained, hbm_peak))
+            if args.nvtx:
+                torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
 
     cpu = None
@@ -503,6 +515,99 @@ def main():
     return 0
 
 
+def run_packed16k_seeds(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                        bf16_sustained, hbm_peak):
+    """The packed 16K forward (plan + cpattn_fwd fused) on seeds 0, 1 and 2 of
+    the workload: seed 0 plans every sample at CP 1, seed 1 two samples at
+    CP 2, seed 2 one at CP 4.  Each seed's attention kernel timed alone (CUDA
+    events over the launches), as the headline roofline is."""
+    import numpy as np
+    w = workloads.WORKLOADS[WORKLOAD]
+    H, D = w["H"], w["D"]
+    res = {}
+    steps = max(5, min(args.steps, 20))
+    for seed in (0, 1, 2):
+        lengths = workloads.packed_lengths(seed, w["budget"])
+        plan = cpattn.plan(lengths, w["world"], w["limit"], w["max_cp"])
+        cps_l = [int(c) for c in plan["cp_size"]]
+        T = sum(lengths)
+        q, k, v = workloads.qkv_device(T, H, D, seed, device=dev)
+        cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+        cps = torch.tensor(cps_l, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        ws = cpattn.alloc_workspace(T, len(lengths), H, D, w["max_cp"], cpattn.MODE_FUSED,
+                                    device=dev)
+        fn = lambda: cpattn.fwd(q, k, v, cu, cps, max_seqlen=max(lengths),  # noqa: E731
+                                max_cp=w["max_cp"], softmax_scale=1.0 / np.sqrt(D), out=out,
+                                lse=lse, workspace=ws)
+        clocks.mark(True)
+        ms = time_loop(torch, fn, steps, 3, stream)
+        clocks.mark(False)
+        assert cpattn.poll_error(ws) == cpattn.OK
+        flops = attention_flops(lengths, H, D)
+        tf = flops / (ms * 1e-3) / 1e12
+        res[str(seed)] = {"lengths": lengths, "cp_sizes": cps_l, "flops": flops,
+                          "kernel_ms": ms, "tflops": tf, "frac": tf / bf16_peak}
+        del q, k, v, out, lse, ws
+    torch.cuda.empty_cache()
+    return {"packed16k_seeds": {"what": "attention kernel (+ schedule kernel) alone per seed "
+                                        "of the packed 16K workload; seed 0 is the headline",
+                                **res}}
+
+
+def cpu_oracle_long128k(budget_rows=4096):
+    """The float64 oracle's full attention on the first ``budget_rows`` rows of
+    the 131,072-token causal sequence (H=16, D=128, N(0, 0.5^2)): under
+    causality those rows see only keys among themselves, so this is the
+    oracle's computation for that labelled subset of the workload; the rate
+    (TFLOP/s over the subset's visible pairs) is what the whole sequence would
+    run at on these cores, and the time for the whole is extrapolated."""
+    import numpy as np
+    from long_context_gb300 import workloads
+    from oracle import attention as oa
+    w = workloads.WORKLOADS["long128k"]
+    H, D, L = w["H"], w["D"], w["lengths"][0]
+    n = budget_rows
+    q, k, v = workloads.qkv(n, H, D, 0, std=w["std"])
+    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
+    cu = np.array([0, n], dtype=np.int64)
+    t0 = time.perf_counter()
+    oa.full_attention(qf, kf, vf, cu, 1.0 / np.sqrt(D))
+    dt = time.perf_counter() - t0
+    tf = attention_flops([n], H, D) / dt / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "float64 oracle full attention over rows 0..%d of the causal %d-token "
+                      "sequence (they see only each other), H=%d, D=%d: %.1f s; the whole "
+                      "sequence at this rate: %.0f s" % (n - 1, L, H, D, dt,
+                                                          attention_flops([L], H, D) / tf / 1e12)}
+
+
+def cpu_oracle_merge8(rows=65536):
+    """The float64 oracle's step-by-step merge on ``rows`` (token, head) rows of
+    the CP=8 merge workload (S=8, D=128 fp32 partials); rate in GB/s of the
+    merge's algorithmic bytes, extrapolated to the whole 4.9 GB."""
+    import numpy as np
+    from long_context_gb300 import workloads
+    from oracle import attention as oa
+    w = workloads.WORKLOADS["merge8"]
+    S, D = w["S"], w["D"]
+    o, m, l = workloads.merge_partials(S, rows, 1, D, seed=0)
+    o, m, l = (x.numpy() for x in (o, m, l))
+    t0 = time.perf_counter()
+    oa.merge_partials(o, m, l)
+    dt = time.perf_counter() - t0
+    nbytes = S * rows * (D + 2) * 4 + rows * (D + 2) * 4
+    gbs = nbytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    total = S * w["T"] * w["H"] * (D + 2) * 4 + w["T"] * w["H"] * (D + 2) * 4
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "float64 oracle merge (step-by-step fold) of %d rows of the CP=8 "
+                      "partials, D=%d: %.2f s; the whole %.1f GB at this rate: %.0f s"
+                      % (rows, D, dt, total / 1e9, total / gbs / 1e9)}
+
+
 def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                  bf16_sustained, hbm_peak):
     import numpy as np
@@ -536,6 +641,8 @@ def run_long128k(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     res["long128k"] = {"workload": "one causal %d-token sequence, CP=4 (%d-token chunks), "
                                    "H=16, D=128, bf16 N(0,0.5^2)" % (L, L // c),
                        "flops": flops, "steps": steps, **sub}
+    if args.rank == 0 and not args.no_cpu_baseline:
+        res["long128k"]["cpu_baseline"] = cpu_oracle_long128k()
     del q, k, v, out, lse
     torch.cuda.empty_cache()
     return res
@@ -766,6 +873,47 @@ def run_sweep256(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                          "launches_per_step": 2 * n_mb}}
 
 
+def run_dcp_sweep256(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
+                     bf16_sustained, hbm_peak):
+    """The 256-sample sweep run the dynamic-CP way (cpattn.DcpForward): the
+    whole mini-batch resident in original order, and per planned micro-batch
+    select Q/K/V into packed arrays, the forward at the planned CP sizes, and O
+    and LSE restored to the original rows -- no host synchronisation inside
+    the step.  Compare with ``sweep256`` (the same forwards on inputs already
+    packed per micro-batch): the difference is the DCP data movement."""
+    import numpy as np
+    w = workloads.WORKLOADS["sweep256"]
+    H, D = w["H"], w["D"]
+    lengths = workloads.uniform_lengths(args.seed, w["n"], w["lo"], w["hi"])
+    plan = cpattn.plan(lengths, w["world"], w["limit"], w["max_cp"])
+    T = sum(lengths)
+    q, k, v = workloads.qkv_device(T, H, D, args.seed, device=dev)
+    cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    run = cpattn.DcpForward(lengths, plan, num_heads=H, head_dim=D, max_cp=w["max_cp"],
+                            device=dev)
+    fn = lambda: run(q, k, v, cu, softmax_scale=1.0 / np.sqrt(D), out=out,  # noqa: E731
+                     lse=lse)
+    clocks.mark(True)
+    ms = time_loop(torch, fn, max(2, min(args.steps, 3)), 1, stream)
+    clocks.mark(False)
+    assert cpattn.poll_error(run.workspace) == cpattn.OK
+    assert int(run.status.item()) == 0
+    flops = attention_flops(lengths, H, D)
+    tf = flops / (ms * 1e-3) / 1e12
+    moved = 2 * (3 * T * H * D * 2) + 2 * (T * H * D * 2 + T * H * 4)
+    n_mb = len(run.micro)
+    del q, k, v, out, lse, run
+    torch.cuda.empty_cache()
+    return {"dcp_sweep256": {"workload": "the 256-sample sweep (%d tokens) through "
+                                         "cpattn.DcpForward: select, forward, restore per "
+                                         "micro-batch (%d), H=32, D=128" % (T, n_mb),
+                             "ms": ms, "tflops": tf, "frac_of_burst": tf / bf16_peak,
+                             "permute_bytes": moved,
+                             "launches_per_step": 7 * n_mb}}
+
+
 def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
                bf16_sustained, hbm_peak):
     res = {}
@@ -789,6 +937,8 @@ def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     res["merge8"] = {"workload": "CP=8 partials, T=32768, H=32, D=128 fp32 (inputs 4.4 GB > L2)",
                      "bytes": nbytes, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
                      "traffic": profiled_traffic("merge_merge8.md", "merge.cu")}
+    if args.rank == 0 and not args.no_cpu_baseline:
+        res["merge8"]["cpu_baseline"] = cpu_oracle_merge8()
     del o, m, l, oo, om, ol
     torch.cuda.empty_cache()
     return res

@@ -10,6 +10,7 @@ library's kernels; there is no fallback.  Importing this module raises
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 
@@ -30,6 +31,7 @@ ERR_WORKSPACE_TOO_SMALL = 3
 ERR_PLAN_INFEASIBLE = 4
 ERR_CUDA = 5
 ERR_DEVICE_TIMEOUT = 6
+ERR_DEVICE_BOUNDS = 7
 MODE_FUSED = 0
 MODE_UNFUSED = 1
 
@@ -95,6 +97,39 @@ class CpattnError(RuntimeError):
         super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
 
 
+# ---------------------------------------------------------------- tracing --
+# NVTX ranges around every public call (named after the C entry point), for
+# profilers that filter or group by range (e.g. ncu --nvtx --nvtx-include
+# "cpattn_fwd/").  Off by default -- a disabled range costs one flag test --
+# and switched on by set_tracing(True) or CPATTN_NVTX=1 in the environment.
+_TRACE = os.environ.get("CPATTN_NVTX", "") not in ("", "0")
+
+
+def set_tracing(enabled):
+    """Switch the NVTX ranges around the public calls on or off."""
+    global _TRACE
+    _TRACE = bool(enabled)
+
+
+def tracing():
+    return _TRACE
+
+
+def _traced(name):
+    def deco(fn):
+        @functools.wraps(fn)
+        def wrapper(*args, **kwargs):
+            if not _TRACE:
+                return fn(*args, **kwargs)
+            torch.cuda.nvtx.range_push(name)
+            try:
+                return fn(*args, **kwargs)
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return wrapper
+    return deco
+
+
 def status_string(status):
     return _lib.cpattn_status_string(int(status)).decode()
 
@@ -138,6 +173,7 @@ def _need(t, name, dtype, device=None, shape=None):
 
 # ---------------------------------------------------------------- planner --
 
+@_traced("cpattn_plan")
 def plan(seqlens, dpxcp_world_size, max_seqlen_per_dp_cp_rank, max_cp):
     """``cpattn_plan`` on host arrays; returns a dict of NumPy int32 arrays.
 
@@ -184,6 +220,18 @@ def alloc_workspace(total_tokens, num_seqs, num_heads, head_dim, max_cp, mode=MO
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def _max_cp(cp_size, max_cp):
+    """``max_cp`` as given; 1 when there are no CP sizes.  With device CP sizes
+    and no ``max_cp`` the call is refused: finding their maximum would read
+    device memory and synchronise the host with the stream."""
+    if max_cp is not None:
+        return int(max_cp)
+    if cp_size is None or cp_size.numel() == 0:
+        return 1
+    raise ValueError("max_cp is required when cp_size is given (an upper bound on the CP "
+                     "sizes, e.g. the planner's max_cp)")
+
+
 def _fwd_common(q, k, v, cu_seqlens, cp_size):
     _need(q, "q", torch.bfloat16)
     if q.dim() != 3:
@@ -199,6 +247,7 @@ def _fwd_common(q, k, v, cu_seqlens, cp_size):
     return dev
 
 
+@_traced("cpattn_fwd")
 def fwd(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None, softmax_scale=None,
         causal=True, mode=MODE_FUSED, out=None, lse=None, workspace=None, stream=None):
     """Ring-attention forward (``cpattn_fwd``); returns ``(out, lse)``.
@@ -210,8 +259,7 @@ def fwd(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None, softmax_s
     dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
     T, H, D = q.shape
     B = cu_seqlens.numel() - 1
-    if max_cp is None:
-        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    max_cp = _max_cp(cp_size, max_cp)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -232,6 +280,7 @@ def fwd(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None, softmax_s
     return out, lse
 
 
+@_traced("cpattn_fwd_noalloc")
 def fwd_noalloc(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
                 softmax_scale=None, causal=True, out, lse=None, status=None, stream=None):
     """``cpattn_fwd_noalloc``: the fused forward with the library's fixed
@@ -242,8 +291,7 @@ def fwd_noalloc(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
     dev = _fwd_common(q, k, v, cu_seqlens, cp_size)
     T, H, D = q.shape
     B = cu_seqlens.numel() - 1
-    if max_cp is None:
-        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    max_cp = _max_cp(cp_size, max_cp)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     _need(out, "out", torch.bfloat16, dev, q.shape)
@@ -259,6 +307,7 @@ def fwd_noalloc(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
     return out, lse
 
 
+@_traced("cpattn_fwd_partials")
 def fwd_partials(q, k, v, cu_seqlens, cp_size=None, *, max_seqlen, max_cp, num_steps=None,
                  softmax_scale=None, causal=True, o_steps=None, m_steps=None, l_steps=None,
                  workspace=None, stream=None):
@@ -305,6 +354,7 @@ def alloc_bwd_workspace(total_tokens, num_seqs, num_heads, head_dim, max_cp, dev
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+@_traced("cpattn_bwd")
 def bwd(q, k, v, out, dout, lse, cu_seqlens, cp_size=None, *, max_seqlen, max_cp=None,
         softmax_scale=None, causal=True, dq=None, dk=None, dv=None, workspace=None,
         stream=None):
@@ -320,8 +370,7 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens, cp_size=None, *, max_seqlen, max_cp
     _need(out, "out", torch.bfloat16, dev, q.shape)
     _need(dout, "dout", torch.bfloat16, dev, q.shape)
     _need(lse, "lse", torch.float32, dev, (T, H))
-    if max_cp is None:
-        max_cp = 1 if cp_size is None else int(cp_size.max().item()) if B else 1
+    max_cp = _max_cp(cp_size, max_cp)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     grads = []
@@ -344,21 +393,31 @@ def bwd(q, k, v, out, dout, lse, cu_seqlens, cp_size=None, *, max_seqlen, max_cp
 
 # -------------------------------------------------------- DCP data movement --
 
-def select_cu(cu_seqlens, ids, *, stream=None):
+@_traced("cpattn_select_cu")
+def select_cu(cu_seqlens, ids, *, out=None, status=None, stream=None):
     """``cpattn_select_cu``: cu_seqlens of the packed selection of samples
     ``ids`` (device int32).  Returns ``(pack_cu, status)`` (device int32
-    tensors; status 0 when every id is valid)."""
+    tensors, ``out`` / ``status`` if given; status 0 when every id is valid)."""
     _need(cu_seqlens, "cu_seqlens", torch.int32)
     _need(ids, "ids", torch.int32, cu_seqlens.device)
     n = ids.numel()
-    pack_cu = torch.empty(n + 1, dtype=torch.int32, device=cu_seqlens.device)
-    status = torch.empty(1, dtype=torch.int32, device=cu_seqlens.device)
+    dev = cu_seqlens.device
+    if out is None:
+        out = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    else:
+        _need(out, "out", torch.int32, dev, (n + 1,))
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    else:
+        _need(status, "status", torch.int32, dev, (1,))
+    pack_cu = out
     st = _lib.cpattn_select_cu(_ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(ids), n,
                                _ptr(pack_cu), _ptr(status), _stream(stream))
     _check(st, "cpattn_select_cu")
     return pack_cu, status
 
 
+@_traced("cpattn_permute_samples")
 def permute_samples(src, orig_cu, pack_cu, ids, status, *, gather, dst, stream=None):
     """``cpattn_permute_samples`` on token-major tensors (``[T, ...]``, rows
     contiguous): ``gather=True`` copies samples ``ids`` of the original
@@ -377,45 +436,110 @@ def permute_samples(src, orig_cu, pack_cu, ids, status, *, gather, dst, stream=N
     return dst
 
 
-def dcp_fwd(q, k, v, cu_seqlens, plan_result, *, max_cp, softmax_scale=None, causal=True,
-            stream=None):
-    """The forward run the dynamic-CP way on one device: for every micro-batch
-    of ``plan_result`` (from :func:`plan` on the same lengths), select its
-    samples into packed arrays (``cpattn_select_cu``, ``cpattn_permute_samples``),
-    run ``cpattn_fwd`` at the planned CP sizes, and restore O and LSE to the
-    original sample order.  Returns ``(out, lse)`` in the original order."""
-    dev = _fwd_common(q, k, v, cu_seqlens, None)
-    T, H, D = q.shape
-    out = torch.empty_like(q)
-    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    mb = np.asarray(plan_result["micro_batch"])
-    order = np.asarray(plan_result["order"])
-    cps = np.asarray(plan_result["cp_size"])
-    lengths = np.diff(cu_seqlens.cpu().numpy())
-    for m in range(int(plan_result["num_micro_batches"])):
-        sel = [int(b) for b in order if mb[b] == m]
-        ids = torch.tensor(sel, dtype=torch.int32, device=dev)
-        pack_cu, status = select_cu(cu_seqlens, ids, stream=stream)
-        rows = int(sum(lengths[b] for b in sel))
-        packed = []
-        for x in (q, k, v):
-            buf = torch.empty((rows, H, D), dtype=x.dtype, device=dev)
-            permute_samples(x, cu_seqlens, pack_cu, ids, status, gather=True, dst=buf,
+class DcpForward:
+    """The forward run the dynamic-CP way on one device, prepared once per
+    plan ("Dynamic Context Parallelism (DCP)": every rank sees the same
+    samples, selects its own, and the output order is restored afterwards).
+
+    For every micro-batch of ``plan_result`` (from :func:`plan` on the host
+    lengths ``seqlens``) a call selects the micro-batch's samples into packed
+    arrays (``cpattn_select_cu``, ``cpattn_permute_samples``), runs
+    ``cpattn_fwd`` at the planned CP sizes and writes O and LSE back to the
+    samples' original rows.  Everything a call needs from the plan is worked
+    out here on the host and uploaded once; the packed buffers and the
+    forward's workspace are allocated once at the largest micro-batch.  A
+    call therefore only enqueues kernels: it never reads device memory, so it
+    does not wait for the stream.  Calls on one object share its buffers:
+    run them in stream order (one stream), not concurrently.
+    """
+
+    def __init__(self, seqlens, plan_result, *, num_heads, head_dim, max_cp, device=None):
+        lengths = [int(x) for x in seqlens]
+        dev = torch.device(device or "cuda")
+        mb = np.asarray(plan_result["micro_batch"])
+        order = np.asarray(plan_result["order"])
+        cps = np.asarray(plan_result["cp_size"])
+        if len(mb) != len(lengths):
+            raise ValueError("plan_result does not match seqlens")
+        self.H, self.D, self.max_cp, self.dev = int(num_heads), int(head_dim), int(max_cp), dev
+        self.B, self.T = len(lengths), sum(lengths)
+        self.micro = []
+        ids_all, cps_all = [], []
+        for m in range(int(plan_result["num_micro_batches"])):
+            sel = [int(b) for b in order if mb[b] == m]
+            if not sel:
+                continue
+            self.micro.append(dict(off=len(ids_all), n=len(sel),
+                                   rows=sum(lengths[b] for b in sel),
+                                   max_seqlen=max(max(lengths[b] for b in sel), 1)))
+            ids_all += sel
+            cps_all += [int(cps[b]) for b in sel]
+        if any(c > self.max_cp for c in cps_all):
+            raise ValueError("a planned CP size exceeds max_cp")
+        host = torch.tensor([ids_all, cps_all], dtype=torch.int32).reshape(2, -1)
+        if dev.type == "cuda":
+            host = host.pin_memory()
+        dev_arr = host.to(dev, non_blocking=True)
+        self.ids, self.cps = dev_arr[0], dev_arr[1]
+        self.pack_cu = torch.empty(len(ids_all) + len(self.micro), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        rows = max([x["rows"] for x in self.micro] + [0])
+        nmax = max([x["n"] for x in self.micro] + [0])
+        self.packed = [torch.empty((rows, self.H, self.D), dtype=torch.bfloat16, device=dev)
+                       for _ in range(4)]   # Q, K, V, O
+        self.packed_lse = torch.empty((rows, self.H), dtype=torch.float32, device=dev)
+        self.workspace = alloc_workspace(rows, nmax, self.H, self.D, self.max_cp, MODE_FUSED,
+                                         dev)
+        self._host = host  # keeps the pinned source of the upload alive
+
+    @_traced("cpattn.DcpForward")
+    def __call__(self, q, k, v, cu_seqlens, *, softmax_scale=None, causal=True, out=None,
+                 lse=None, stream=None):
+        """Returns ``(out, lse)`` in the original sample order."""
+        dev = _fwd_common(q, k, v, cu_seqlens, None)
+        T, H, D = q.shape
+        if (T, H, D) != (self.T, self.H, self.D) or cu_seqlens.numel() != self.B + 1:
+            raise ValueError("q, k, v, cu_seqlens do not match the planned batch")
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        for i, x in enumerate(self.micro):
+            ids = self.ids[x["off"]:x["off"] + x["n"]]
+            cp_m = self.cps[x["off"]:x["off"] + x["n"]]
+            pack_cu = self.pack_cu[x["off"] + i:x["off"] + i + x["n"] + 1]
+            select_cu(cu_seqlens, ids, out=pack_cu, status=self.status, stream=stream)
+            rows = x["rows"]
+            pq, pk, pv, po = (b[:rows] for b in self.packed)
+            pl = self.packed_lse[:rows]
+            for src, dst in ((q, pq), (k, pk), (v, pv)):
+                permute_samples(src, cu_seqlens, pack_cu, ids, self.status, gather=True,
+                                dst=dst, stream=stream)
+            fwd(pq, pk, pv, pack_cu, cp_m, max_seqlen=x["max_seqlen"], max_cp=self.max_cp,
+                softmax_scale=softmax_scale, causal=causal, out=po, lse=pl,
+                workspace=self.workspace, stream=stream)
+            permute_samples(po, cu_seqlens, pack_cu, ids, self.status, gather=False, dst=out,
                             stream=stream)
-            packed.append(buf)
-        cp_m = torch.tensor([int(cps[b]) for b in sel], dtype=torch.int32, device=dev)
-        o_m, l_m = fwd(*packed, pack_cu, cp_m, max_seqlen=int(max(lengths[b] for b in sel)),
-                       max_cp=max_cp, softmax_scale=softmax_scale, causal=causal,
-                       stream=stream)
-        permute_samples(o_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=out,
-                        stream=stream)
-        permute_samples(l_m, cu_seqlens, pack_cu, ids, status, gather=False, dst=lse,
-                        stream=stream)
-    return out, lse
+            permute_samples(pl, cu_seqlens, pack_cu, ids, self.status, gather=False, dst=lse,
+                            stream=stream)
+        return out, lse
+
+
+@_traced("cpattn.dcp_fwd")
+def dcp_fwd(q, k, v, cu_seqlens, plan_result, *, seqlens, max_cp, softmax_scale=None,
+            causal=True, stream=None):
+    """One-shot :class:`DcpForward`: plan-derived buffers built for this call
+    (``seqlens`` are the host lengths the plan was made from).  Returns
+    ``(out, lse)`` in the original sample order."""
+    T, H, D = q.shape
+    run = DcpForward(seqlens, plan_result, num_heads=H, head_dim=D, max_cp=max_cp,
+                     device=q.device)
+    return run(q, k, v, cu_seqlens, softmax_scale=softmax_scale, causal=causal, stream=stream)
 
 
 # ---------------------------------------------------------------- Ulysses --
 
+@_traced("cpattn_ulysses_layout")
 def ulysses_layout(src, sp_size, *, to_head_groups, dst=None, stream=None):
     """``cpattn_ulysses_layout``.  ``to_head_groups=True``: ``src [T, H, ...]``
     -> ``[P, T, H / P, ...]``; ``False``: ``src [P, T, H / P, ...]`` ->
@@ -445,6 +569,7 @@ def ulysses_layout(src, sp_size, *, to_head_groups, dst=None, stream=None):
     return dst
 
 
+@_traced("cpattn_ulysses_seqlens")
 def ulysses_seqlens(cu_seqlens, cp_size, sp_size, num_tokens, *, stream=None):
     """``cpattn_ulysses_seqlens``: cu_seqlens and cp_size of the head-group
     layout as one packed batch of ``sp_size * B`` samples."""
@@ -462,6 +587,7 @@ def ulysses_seqlens(cu_seqlens, cp_size, sp_size, num_tokens, *, stream=None):
     return cu_out, cp_out
 
 
+@_traced("cpattn.ulysses_fwd")
 def ulysses_fwd(q, k, v, cu_seqlens, sp_size, cp_size=None, *, max_seqlen, max_cp=None,
                 softmax_scale=None, causal=True, stream=None):
     """Attention the Ulysses way on one device: Q, K, V to the head-group
@@ -476,8 +602,7 @@ def ulysses_fwd(q, k, v, cu_seqlens, sp_size, cp_size=None, *, max_seqlen, max_c
     grouped = [ulysses_layout(x, P, to_head_groups=True, stream=stream).view(P * T, H // P, D)
                for x in (q, k, v)]
     cu_g, cp_g = ulysses_seqlens(cu_seqlens, cp_size, P, T, stream=stream)
-    if max_cp is None:
-        max_cp = 1 if cp_size is None or cp_size.numel() == 0 else int(cp_size.max().item())
+    max_cp = _max_cp(cp_size, max_cp)
     o_g, l_g = fwd(*grouped, cu_g, cp_g, max_seqlen=max_seqlen, max_cp=max_cp,
                    softmax_scale=softmax_scale, causal=causal, stream=stream)
     out = ulysses_layout(o_g.view(P, T, H // P, D), P, to_head_groups=False, stream=stream)
@@ -500,6 +625,7 @@ def _decode_check(q, k, v, cu_seqlens):
     return dev
 
 
+@_traced("cpattn_decode_partials")
 def decode_partials(q, k, v, cu_seqlens, *, cp, softmax_scale=None, stream=None):
     """``cpattn_decode_partials``: returns ``(o_steps [cp, B, H, D] fp32,
     lse_steps [cp, B, H] fp32)``."""
@@ -516,6 +642,7 @@ def decode_partials(q, k, v, cu_seqlens, *, cp, softmax_scale=None, stream=None)
     return o_s, l_s
 
 
+@_traced("cpattn_merge_lse")
 def merge_lse(o_steps, lse_steps, *, stream=None):
     """``cpattn_merge_lse`` over the leading axis of normalised partials
     ``o_steps [S, ..., D]`` and ``lse_steps [S, ...]``; returns ``(O, LSE)``."""
@@ -531,6 +658,7 @@ def merge_lse(o_steps, lse_steps, *, stream=None):
     return out, lse
 
 
+@_traced("cpattn_decode")
 def decode(q, k, v, cu_seqlens, *, cp, softmax_scale=None, out=None, lse=None, workspace=None,
            stream=None):
     """``cpattn_decode``: decode-time CP attention; returns ``(out bf16 [B, H, D],
@@ -555,6 +683,7 @@ def decode(q, k, v, cu_seqlens, *, cp, softmax_scale=None, out=None, lse=None, w
     return out, lse
 
 
+@_traced("cpattn_merge")
 def merge(o_steps, m_steps, l_steps, *, out_o=None, out_m=None, out_l=None, stream=None):
     """Fold stored partials (``cpattn_merge``); returns ``(O / l, m, l)`` in fp32."""
     _need(o_steps, "o_steps", torch.float32)

@@ -167,3 +167,21 @@ def test_ulysses_argument_errors_return_before_launch(cp):
     assert s(a, None, 2, 8, 0, b, None, None) == 1         # sp_size 0
     assert s(None, None, 2, 8, 2, b, None, None) == 1      # no cu_seqlens
     assert s(a, None, 2, 1 << 30, 4, b, None, None) == 1   # P T >= 2^31
+
+
+def test_tracing_ranges_wrap_public_calls():
+    """With tracing on, the planner call runs inside an NVTX range (pushed and
+    popped around it, also when it raises) and returns the same result."""
+    from long_context_gb300 import cpattn
+    base = cpattn.plan([100, 5000, 30], 4, 4096, 4)
+    was = cpattn.tracing()
+    try:
+        cpattn.set_tracing(True)
+        traced = cpattn.plan([100, 5000, 30], 4, 4096, 4)
+        with pytest.raises(cpattn.CpattnError):
+            cpattn.plan([100, 50000], 4, 4096, 4)
+    finally:
+        cpattn.set_tracing(was)
+    for key in ("cp_size", "micro_batch", "first_rank", "order"):
+        assert list(traced[key]) == list(base[key])
+    assert cpattn.plan.__name__ == "plan" and cpattn.fwd.__name__ == "fwd"
