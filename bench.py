@@ -305,19 +305,38 @@ def main():
     scale = 1.0 / np.sqrt(D)
     q, k, v = workloads.qkv_device(T, H, D, seed, device=dev)
     cu = torch.from_numpy(workloads.cu_seqlens(lengths)).to(dev)
-    cp_pinned = torch.zeros(B, dtype=torch.int32).pin_memory()
-    cp_dev = torch.zeros(B, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     ws = cpattn.alloc_workspace(T, B, H, D, max_cp, cpattn.MODE_FUSED, device=dev)
     flops = attention_flops(lengths, H, D)
+    # The plan goes up the way a caller streaming micro-batches sends it:
+    # two pinned host / device buffer pairs and a copy stream, so that step
+    # i's CP sizes are uploaded while step i-1's kernels run (the forward
+    # waits on an event for its own upload; an upload waits until the forward
+    # two steps back has finished reading that buffer).
+    NP = 2
+    cp_pinned = [torch.zeros(B, dtype=torch.int32).pin_memory() for _ in range(NP)]
+    cp_bufs = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(NP)]
+    cp_dev = cp_bufs[0]
+    s_plan = torch.cuda.Stream(device=dev)
+    ev_up = [torch.cuda.Event() for _ in range(NP)]
+    ev_read = [torch.cuda.Event() for _ in range(NP)]
+    n_step = [0]
 
     def step():
+        b_ = n_step[0] % NP
+        n_step[0] += 1
         plan = cpattn.plan(lengths, W, limit, max_cp)           # dynamic-CP plan (host)
-        cp_pinned.numpy()[:] = plan["cp_size"]
-        cp_dev.copy_(cp_pinned, non_blocking=True)
-        cpattn.fwd(q, k, v, cu, cp_dev, max_seqlen=max(lengths), max_cp=max_cp,
+        ev_up[b_].synchronize()          # this pinned buffer's last upload is done
+        cp_pinned[b_].numpy()[:] = plan["cp_size"]
+        with torch.cuda.stream(s_plan):
+            s_plan.wait_event(ev_read[b_])
+            cp_bufs[b_].copy_(cp_pinned[b_], non_blocking=True)
+            ev_up[b_].record(s_plan)
+        stream.wait_event(ev_up[b_])
+        cpattn.fwd(q, k, v, cu, cp_bufs[b_], max_seqlen=max(lengths), max_cp=max_cp,
                    softmax_scale=scale, out=out, lse=lse, workspace=ws)
+        ev_read[b_].record(stream)
 
     def kernel_only():
         cpattn.fwd(q, k, v, cu, cp_dev, max_seqlen=max(lengths), max_cp=max_cp,
