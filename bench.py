@@ -170,32 +170,40 @@ def dist_setup(args):
 
 # ------------------------------------------------------------ reference --
 
+def _oracle_head_batch(lengths, H, D, seed):
+    """The batch's Q, K, V (bf16 bytes the GPU sees, seeded) and cu_seqlens;
+    the oracle takes them one head at a time."""
+    from long_context_gb300 import workloads
+    T = sum(lengths)
+    q, k, v = workloads.qkv(T, H, D, seed)
+    return q, k, v, workloads.cu_seqlens(lengths)
+
+
 def cpu_oracle_sample(lengths, H, D, seed, budget_s):
-    """Time the float64 oracle's full attention on the batch's shortest samples
-    until about ``budget_s`` seconds of work; returns (TFLOP/s, desc, cores)."""
+    """Time the float64 oracle's full attention over every sample of the
+    batch, one head at a time, until about ``budget_s`` seconds of work (each
+    head is the batch's whole length mix); returns (TFLOP/s, desc, cores,
+    seconds)."""
     import numpy as np
     from long_context_gb300 import workloads
     from oracle import attention as oa
-    order = sorted(range(len(lengths)), key=lambda b: lengths[b])
-    flops = 0.0
-    used = []
-    t_total = 0.0
+    q, k, v, cu = _oracle_head_batch(lengths, H, D, seed)
     scale = 1.0 / np.sqrt(D)
-    for b in order:
-        L = lengths[b]
-        q, k, v = workloads.qkv(L, H, D, seed + 7919 * b)
-        qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
-        cu = np.array([0, L], dtype=np.int64)
+    flops, t_total, heads = 0.0, 0.0, 0
+    for h in range(H):
+        sl = slice(h, h + 1)
+        qf, kf, vf = (workloads.to_f64(x[:, sl]) for x in (q, k, v))
         t0 = time.perf_counter()
         oa.full_attention(qf, kf, vf, cu, scale)
         t_total += time.perf_counter() - t0
-        flops += attention_flops([L], H, D)
-        used.append(L)
+        flops += attention_flops(lengths, 1, D)
+        heads += 1
         if t_total >= budget_s:
             break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    desc = ("float64 oracle full attention (NumPy/BLAS) on %d of the batch's samples, "
-            "lengths %s, H=%d, D=%d; %.1f s" % (len(used), used, H, D, t_total))
+    desc = ("float64 oracle full attention (NumPy/BLAS) over every sample of the batch "
+            "(lengths %s), %d of its %d heads, D=%d; %.1f s" % (list(lengths), heads, H, D,
+                                                              t_total))
     return flops / t_total / 1e12, desc, cores, t_total
 
 
@@ -225,22 +233,27 @@ def run_reference(args, rank, world):
     from oracle import attention as oa
     from oracle import planner as op
     plan = op.plan(lengths, w["world"], w["limit"], w["max_cp"])
-    # One step = the oracle's full attention on the batch's shortest sample.
-    L = min(lengths)
-    q, k, v = workloads.qkv(L, H, D, args.seed)
-    qf, kf, vf = (workloads.to_f64(x) for x in (q, k, v))
-    cu = np.array([0, L], dtype=np.int64)
+    # One step = the oracle's full attention over every sample of the batch
+    # for one head (the next head each step): the batch's whole length mix
+    # at 1/H of its work.
+    q, k, v, cu = _oracle_head_batch(lengths, H, D, args.seed)
     scale = 1.0 / np.sqrt(D)
-    for _ in range(args.warmup):
+
+    def one_step(i):
+        sl = slice(i % H, i % H + 1)
+        qf, kf, vf = (workloads.to_f64(x[:, sl]) for x in (q, k, v))
+        t0 = time.perf_counter()
         oa.full_attention(qf, kf, vf, cu, scale)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oa.full_attention(qf, kf, vf, cu, scale)
-    dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    value = attention_flops([L], H, D) / dt / 1e12
+        return time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        one_step(i)
+    dt = sum(one_step(args.warmup + i) for i in range(args.steps)) / max(args.steps, 1)
+    value = attention_flops(lengths, 1, D) / dt / 1e12
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    sample = ("float64 oracle full attention on the batch's shortest sample (L=%d of %s), "
-              "H=%d, D=%d, causal" % (L, lengths, H, D))
+    sample = ("float64 oracle full attention over every sample of the batch (lengths %s), "
+              "one of its %d heads per step, D=%d, causal; rate = that head's FLOPs over "
+              "the oracle's time" % (list(lengths), H, D))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
