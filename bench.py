@@ -53,7 +53,7 @@ def parse_args():
                          "(for profilers that filter by range)")
     ap.add_argument("--small", action="store_true",
                     help="profiling aid: the long-sequence forward and backward (one "
-                         "32768-token sequence), dcp, decode and ulysses measurements on "
+                         "32768-token sequence), merge, dcp, decode and ulysses measurements on "
                          "smaller inputs (each array still larger than L2); not a benchmark "
                          "configuration")
     ap.add_argument("--only", default=None,
@@ -953,6 +953,8 @@ def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     # Merge of CP=8 stored partials, T=32768, H=32, D=128.
     w = workloads.WORKLOADS["merge8"]
     S, T, H, D = w["S"], w["T"], w["H"], w["D"]
+    if args.small:
+        T = 4096  # profiling aid: 0.54 GB of partials, still larger than L2
     g = torch.Generator(device=dev).manual_seed(args.seed)
     o = torch.randn((S, T, H, D), generator=g, device=dev, dtype=torch.float32)
     m = torch.rand((S, T, H), generator=g, device=dev, dtype=torch.float32) * 10 - 5
@@ -966,7 +968,8 @@ def run_merge8(torch, cpattn, workloads, dev, stream, args, clocks, bf16_peak,
     ms = time_loop(torch, fn, max(steps, 10), 3, stream)
     clocks.mark(False)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    res["merge8"] = {"workload": "CP=8 partials, T=32768, H=32, D=128 fp32 (inputs 4.4 GB > L2)",
+    res["merge8"] = {"workload": "CP=8 partials, T=%d, H=32, D=128 fp32 (inputs %.1f GB > L2)"
+                                 % (T, S * T * H * (D + 2) * 4 / 1e9),
                      "bytes": nbytes, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
                      "traffic": profiled_traffic("merge_merge8.md", "merge.cu")}
     if args.rank == 0 and not args.no_cpu_baseline:
