@@ -185,11 +185,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   ring.i = rank;
   ring.causal = p.causal;
   ring.num_steps = p.num_steps;
+  // The chunk's query blocks are aligned to its end: block blk covers rows
+  // [q_lo, q_hi) with q_hi = chunk end - (blocks after it) * 256, so only
+  // block 0 can be short, and a short block is the chunk's cheapest (its
+  // rows see the fewest keys) rather than its costliest.  Its Q tiles start
+  // before the chunk (q0 may even be negative: TMA fills those rows with
+  // zeros); the rows before q_lo are computed but never stored.
+  const int qc_lo = min(rank * ring.chunk, ring.L);
   const int qc_hi = min((rank + 1) * ring.chunk, ring.L);
-  const int q0 = min(rank * ring.chunk, ring.L) + blk * kRowsPerItem;
-  ring.q_blk_end = min(q0 + kRowsPerItem, qc_hi);
-  // The second Q tile is skipped when the block has no rows for it.
-  const int nq = (q0 + kBM < ring.q_blk_end) ? kNQ : 1;
+  const int n_blk = cdiv(qc_hi - qc_lo, kRowsPerItem);
+  const int q_hi = qc_hi - (n_blk - 1 - blk) * kRowsPerItem;
+  const int q_lo = max(q_hi - kRowsPerItem, qc_lo);
+  ring.q_blk_end = q_hi;
+  // The first Q tile is skipped when the block has no rows for it.
+  const int nq = (q_lo + kBM < q_hi) ? kNQ : 1;
+  const int q0 = q_hi - nq * kBM;  // first row of Q tile 0
   if (kDebugChecks) {
     // The work entry must address rows of this batch and a valid head, CP
     // size, rank and block (every CTA thread reads the same entry, so the
@@ -199,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                               p.hdr) &&
                     in_bounds(h, 0, p.num_heads, p.hdr) &&
                     in_bounds(geo.c, 1, kMaxCp + 1, p.hdr) &&
-                    in_bounds(rank, 0, geo.c, p.hdr) && in_bounds(q0, 0, qc_hi, p.hdr);
+                    in_bounds(rank, 0, geo.c, p.hdr) && in_bounds(blk, 0, n_blk, p.hdr) &&
+                    in_bounds(q_lo, qc_lo, qc_hi, p.hdr);
     if (!ok) return;
   }
   const int T32 = static_cast<int>(p.total_tokens);
@@ -251,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_kv = l2_policy_evict_last();
     mbar_arrive_expect_tx(q_full, nq * C::kTileBytes);
     for (int t = 0; t < nq; ++t) {
-      const int qrow = checked_coord(tok0 + q0 + t * kBM, 0, T32, p.hdr);
+      const int qrow = checked_coord(tok0 + q0 + t * kBM, -kBM, T32, p.hdr);
       for (int hf = 0; hf < C::kHalves; ++hf)
         tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * 16384, &tm_q, q_full,
                     hf * 64, h, qrow, pol_q);
@@ -300,9 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rankn = wn.w & 0xff;
             const int blkn = static_cast<int>(static_cast<unsigned>(wn.w) >> 8);
             const int chunkn = cdiv(Ln, cn);
-            const int q0n = min(rankn * chunkn, Ln) + blkn * kRowsPerItem;
-            const int qendn = min(q0n + kRowsPerItem, min((rankn + 1) * chunkn, Ln));
-            const int nqn = (q0n + kBM < qendn) ? kNQ : 1;
+            const int qc_lon = min(rankn * chunkn, Ln);
+            const int qc_hin = min((rankn + 1) * chunkn, Ln);
+            const int q_hin = qc_hin - (cdiv(qc_hin - qc_lon, kRowsPerItem) - 1 - blkn) *
+                                           kRowsPerItem;
+            const int nqn = (max(q_hin - kRowsPerItem, qc_lon) + kBM < q_hin) ? kNQ : 1;
+            const int q0n = q_hin - nqn * kBM;
             for (int t = 0; t < nqn; ++t)
               for (int hf = 0; hf < C::kHalves; ++hf)
                 tma_prefetch_l2_3d(&tm_q, hf * 64, hn, wn.x + q0n + t * kBM);
@@ -486,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_addr = tmem + lane_base + t * kBN;
       const uint32_t o_addr = tmem + lane_base + C::kOCol + t * D;
       const int q_pos = q0 + t * kBM + r;
-      const bool row_valid = q_pos < ring.q_blk_end;
+      const bool row_valid = q_pos >= q_lo && q_pos < q_hi;
       const size_t row_idx = static_cast<size_t>(tok0 + q_pos) * p.num_heads + h;
       const float c_log2 = p.scale_log2;
 
@@ -686,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(stage + swizzle128(r, q * 4 + e)) =
                   make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
-          if (q0 + t * kBM + kBM <= ring.q_blk_end) {
+          if (q0 + t * kBM >= q_lo && q0 + t * kBM + kBM <= q_hi) {
             // A full tile: the staged layout is the TMA layout, so one thread
             // stores it with the bulk engine once every row is staged (each
             // thread makes its writes visible to the async proxy first).  The
@@ -710,10 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
           } else {
-            // The tile that ends a chunk: its rows past the chunk belong to
-            // another rank or sample, so the warp copies its own 32 rows out
-            // with D / 8 lanes per row (every store instruction writes whole
-            // rows), skipping those.
+            // The tile that starts a short block: its rows before the block
+            // belong to another block, rank or sample, so the warp copies its
+            // own 32 rows out with D / 8 lanes per row (every store
+            // instruction writes whole rows), skipping those.
             __syncwarp();
             constexpr int kLpr = D / 8;      // lanes per row: one 16-byte chunk each
             constexpr int kRpi = 32 / kLpr;  // rows per store instruction
@@ -724,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rr = row_w + it * kRpi + lane / kLpr;
               const uint4 val = *reinterpret_cast<const uint4*>(stage + swizzle128(rr, c));
               const int qp = q0 + t * kBM + rr;
-              if (qp < ring.q_blk_end && in_bounds(tok0 + qp, 0, p.total_tokens, p.hdr))
+              if (qp >= q_lo && qp < q_hi && in_bounds(tok0 + qp, 0, p.total_tokens, p.hdr))
                 *reinterpret_cast<uint4*>(
                     p.out + (static_cast<size_t>(tok0 + qp) * p.num_heads + h) * D + c * 8) = val;
             }
