@@ -56,6 +56,8 @@ constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;  // warps 0-7
 // Named barriers 3 and 4: the compute warps, warp 10 and the MMA warp.
 constexpr int kHandoffThreads = kComputeThreads + 64;
+// Named barrier 5 (dK/dV kernel): the compute warps and the MMA warp.
+constexpr int kHalfThreads = kComputeThreads + 32;
 // Register split (setmaxnreg): launched at 168 per thread, the compute
 // warpgroups rise to 224 and the control warpgroup drops to 56.
 constexpr int kBwdLaunchRegs = 168;
@@ -81,10 +83,10 @@ struct BwdCfg {
   static constexpr int kA1Off = kTileBytes;
   static constexpr int kB0Off = 2 * kTileBytes;
   static constexpr int kB1Off = kB0Off + S0 * kTileBytes;
-  // dK/dV kernel: per streamed query tile, LSE * log2 e and D of its 128
-  // queries, two buffers (float [2][2][128]).
+  // dK/dV kernel: LSE * log2 e and D of the current streamed query tile's
+  // 128 queries (float [2][128]).
   static constexpr int kVecOff = kB1Off + S1 * kTileBytes;
-  static constexpr int kBarOff = kVecOff + (kWithVec ? 2 * 2 * kT * 4 : 0);
+  static constexpr int kBarOff = kVecOff + (kWithVec ? 2 * kT * 4 : 0);
   // a_full, b0_full[S0], b0_empty[S0], b1_full[S1], b1_empty[S1], s_full,
   // o_done, drain, dp_full
   static constexpr int kNumBars = 1 + 2 * S0 + 2 * S1 + 4;
@@ -94,9 +96,11 @@ struct BwdCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// dK/dV: Q and dO each live from their copy to the end of their tile's MMAs.
+// dK/dV: Q is read twice per tile (S^T = K Q^T, then dK += dS^T Q), so its
+// stage is freed late, after dK; a third Q stage lets the copy of tile x + 1
+// start a whole tile earlier.  dO's stage is freed after dV.
 template <int D>
-using DkdvCfg = BwdCfg<D, 2, 2, true>;
+using DkdvCfg = BwdCfg<D, 3, 2, true>;
 // dQ: K is read twice per tile (S = Q K^T, then dQ += dS K), so its stage is
 // freed late; a third K stage gives its copy a full tile period more.
 template <int D>
@@ -234,6 +238,21 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b, u
            (acc || kk > 0) ? 1u : 0u);
 }
 
+// The half of mma_tmem_a over the K-columns that the compute warps write
+// first (half 0: [0, 32) and [64, 96); half 1: [32, 64) and [96, 128)), so
+// that the product can start before all of A is in TMEM.
+template <int D>
+__device__ __forceinline__ void mma_tmem_a_half(uint32_t d, uint32_t a, uint32_t b, uint32_t hi,
+                                                bool acc, int half) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kT, D, true);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int kk = (j & 1) + 2 * half + 4 * (j >> 1);
+    mma_ts(d, a + kk * 8 + (kk >= 4 ? 32 : 0), pack_u64(b + ((kk * 2048) >> 4), hi), idesc,
+           (acc || j > 0) ? 1u : 0u);
+  }
+}
+
 // Loads a 128-row bf16 tile (rows row0.., head h) into shared memory.  (The
 // debug build checks row0 against the T rows of the tensor.)
 template <int D>
@@ -309,11 +328,11 @@ __device__ __forceinline__ void store_rows_staged(uint32_t taddr, float mul, uin
 // A compute warp's arrival on hand-off barrier `id`: non-blocking while its
 // waits succeed; blocking once one has failed (it then skips its work, and
 // must not run ahead of the barrier).
-__device__ __forceinline__ void handoff(uint32_t id, bool ok) {
+__device__ __forceinline__ void handoff(uint32_t id, bool ok, uint32_t n = kHandoffThreads) {
   if (ok)
-    named_bar_arrive(id, kHandoffThreads);
+    named_bar_arrive(id, n);
   else
-    named_bar_sync(id, kHandoffThreads);
+    named_bar_sync(id, n);
 }
 
 struct UnitIds {
@@ -409,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dp_full = drain + 1;  // dP^T ready (S^T ready is s_full)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
-  float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [buf][lse2 | delta][128]
+  float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [lse2 | delta][128]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -518,10 +537,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t do_lo_mn = dsc.lo_mn(smem_u32(smem + C::kB1Off));
       constexpr uint32_t kStageLo = C::kTileBytes >> 4;
       const int n = count_tiles(ring);
-      // Two hand-offs per query tile x: once P^T(x) is in TMEM, dV(x) and then
+      // Three hand-offs per query tile x: once the first half of P^T(x) (the
+      // compute warps' first 32 columns each) is in TMEM, the half of dV(x)
+      // over those queries; once all of P^T(x) is, the other half and then
       // S^T(x + 1) (which overwrites P^T(x) after dV(x) has read it); once
       // dS^T(x) is in TMEM, dK(x) and then dP^T(x + 1).  The exponentials of
-      // tile x + 1 thus overlap dK(x) and dP^T(x + 1).
+      // tile x + 1 thus overlap dK(x) and dP^T(x + 1), and the second half of
+      // P^T(x) overlaps the first half of dV(x).
       named_bar_sync(1, 64);  // K, V and query tile 0 landed
       if (lane == 0 && n > 0) {
         tc_fence_after();
@@ -537,10 +559,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t q_st1 = static_cast<uint32_t>(x + 1) % C::kStages0;
         const uint32_t do_st = static_cast<uint32_t>(x) % C::kStages1;
         const uint32_t do_st1 = static_cast<uint32_t>(x + 1) % C::kStages1;
+        named_bar_sync(5, kHalfThreads);  // the first half of P^T(x) in TMEM
+        if (lane == 0) {
+          tc_fence_after();
+          mma_tmem_a_half<D>(tmem + 2 * kT, tmem, do_lo_mn + do_st * kStageLo, dsc.hi_mn, x > 0, 0);
+        }
+        __syncwarp();
         named_bar_sync(3, kHandoffThreads);  // P^T(x) in TMEM; query tile x + 1 landed
         if (lane == 0) {
           tc_fence_after();
-          mma_tmem_a<D>(tmem + 2 * kT, tmem, do_lo_mn + do_st * kStageLo, dsc.hi_mn, x > 0);  // dV
+          mma_tmem_a_half<D>(tmem + 2 * kT, tmem, do_lo_mn + do_st * kStageLo, dsc.hi_mn, true, 1);
+          mma_commit(&b1_empty[do_st]);  // dO(x): last read by dV(x)
           if (x + 1 < n) {
             mma_abt<D>(tmem, k_lo, q_lo_k + q_st1 * kStageLo, dsc.hi_k);
             mma_commit(s_full);
@@ -552,7 +581,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           mma_tmem_a<D>(tmem + 3 * kT, tmem + kT, q_lo_mn + q_st * kStageLo, dsc.hi_mn, x > 0);  // dK
           mma_commit(&b0_empty[q_st]);
-          mma_commit(&b1_empty[do_st]);
           if (x == n - 1) mma_commit(o_done);
           if (x + 1 < n) {
             mma_abt<D>(tmem + kT, v_lo, do_lo_k + do_st1 * kStageLo, dsc.hi_k);
@@ -621,20 +649,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     Walk<KRing> w;
     w.start(ring);
+    // Column statistics, one tile ahead: for column r of a tile (query
+    // tile_row + r, if it belongs to the chunk) warps 0-3 load its LSE and
+    // warps 4-7 its D.  The load for tile x + 1 is issued at the top of tile
+    // x and consumed at the top of tile x + 1, so its round trip to L2 or
+    // DRAM overlaps a whole tile's work instead of preceding its exponentials.
+    // One shared-memory buffer: it is rewritten once every compute warp is
+    // done with the previous tile.
+    Walk<KRing> w_next = w;
+    float col_raw = 0.f;
+    bool col_ok = false;
+    auto fetch_col = [&](const Walk<KRing>& wt) {
+      const int qp = wt.tile_row() + r;
+      col_ok = qp < wt.end && in_bounds(u.tok0 + qp, 0, p.total_tokens, p.hdr);
+      if (col_ok) {
+        const size_t ri = static_cast<size_t>(u.tok0 + qp) * p.num_heads + u.h;
+        col_raw = __ldg(ch == 0 ? &p.lse[ri] : &p.delta[ri]);
+      }
+    };
+    if (n > 0) fetch_col(w_next);
     for (int x = 0; x < n; ++x, w.advance(ring)) {
       const int qt0 = w.tile_row();  // first query of the tile (sample position)
-      float* lse_s = vec + (x & 1) * 2 * kT;
-      float* dlt_s = lse_s + kT;
-      {
-        // Column r of this tile (query qt0 + r, if it belongs to the chunk):
-        // warps 0-3 load its LSE, warps 4-7 its D.
-        const int qp = qt0 + r;
-        float val = ch == 0 ? kInf : 0.f;  // +inf LSE: P = 0 outside the chunk
-        if (qp < w.end && in_bounds(u.tok0 + qp, 0, p.total_tokens, p.hdr)) {
-          const size_t ri = static_cast<size_t>(u.tok0 + qp) * p.num_heads + u.h;
-          val = ch == 0 ? __ldg(&p.lse[ri]) * kLog2e : __ldg(&p.delta[ri]);
-        }
-        (ch == 0 ? lse_s : dlt_s)[r] = val;
+      float* lse_s = vec;
+      float* dlt_s = vec + kT;
+      if (x > 0) named_bar_sync(2, kComputeThreads);  // tile x - 1's statistics are read
+      // +inf LSE outside the chunk: P = 0 there.
+      if (ch == 0)
+        lse_s[r] = col_ok ? col_raw * kLog2e : kInf;
+      else
+        dlt_s[r] = col_ok ? col_raw : 0.f;
+      if (x + 1 < n) {
+        w_next.advance(ring);
+        fetch_col(w_next);
       }
       named_bar_sync(2, kComputeThreads);  // the column statistics are in shared memory
 #ifdef CPATTN_FAULT_INJECT_DROP_P
@@ -686,9 +732,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
           tmem_st16(row_addr + ch * 64 + q * 16, pw);
+          if (q == 0) {  // the first half of P^T: dV can start on it
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_arrive(5, kHalfThreads);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
+      } else {
+        named_bar_sync(5, kHalfThreads);
       }
       handoff(3, ok);
       // Phase 2: dS^T = P^T (dP^T - D), stored packed over the dP^T region
