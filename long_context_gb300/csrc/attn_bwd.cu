@@ -14,8 +14,8 @@
 // walks the query chunks that see its key block in the order they visit it
 // (chunk j, j + 1, ...).
 //
-// Both kernels: 384 threads, one CTA per SM (192 KB shared memory, 512 TMEM
-// columns):
+// Both kernels: 384 threads, one CTA per SM (224 KB of shared memory: two
+// stationary and five streamed 32 KB tiles; 512 TMEM columns):
 //   warps 0-7  compute: warps w and w + 4 share the TMEM lanes of quarter w
 //              (thread = one row of the stationary tile), for the first and
 //              the second 64 columns of each streamed tile
@@ -28,7 +28,8 @@
 // barriers: barrier 3 for the first hand-off of each streamed tile and
 // barrier 4 for the second, on which the compute warps arrive (bar.arrive)
 // once their TMEM results are in place and warp 10 once the next tile's copy
-// has landed.  A compute warp whose bounded wait failed switches to bar.sync
+// has landed; in the dK/dV kernel also barrier 5 (compute warps only), once
+// the first half of P^T is in place.  A compute warp whose bounded wait failed switches to bar.sync
 // for its remaining hand-offs, so it cannot arrive twice before a barrier
 // completes, and every warp takes part in every hand-off: the MMA warp always
 // runs to its end.
