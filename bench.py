@@ -491,7 +491,10 @@ def main():
     del hq, hk, hv, bufs, h_out, h_lse
 
     extras = {}
-    if not args.no_extras:
+    # The sub-measurements and the CPU baselines belong to the one-GPU line;
+    # with N ranks only the main step is measured, so the N GPUs are held
+    # for as short a time as possible.
+    if not args.no_extras and world == 1:
         for fn in (run_packed16k_seeds, run_long128k, run_merge8, run_backward,
                    run_dcp_permute, run_decode, run_ulysses, run_sweep256, run_dcp_sweep256):
             if args.nvtx:
@@ -503,7 +506,7 @@ def main():
     clk = clocks.stop()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tflops, desc, cores, _ = cpu_oracle_sample(lengths, H, D, seed, budget_s=12.0)
         cpu = {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": desc}
