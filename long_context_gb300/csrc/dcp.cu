@@ -116,10 +116,18 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(
     const uint8_t* s = src + (gather ? o_row : t) * row_bytes;
     uint8_t* d = dst + (gather ? t : o_row) * row_bytes;
     if (vec16) {
-      // Four 16-byte loads in flight per lane before their stores.
+      // Sixteen 16-byte loads in flight per lane before their stores (a whole
+      // 8 KB row per warp), then four.
       const uint4* s4 = reinterpret_cast<const uint4*>(s);
       uint4* d4 = reinterpret_cast<uint4*>(d);
       int e = lane;
+      for (; e + 15 * 32 < n_vec; e += 16 * 32) {
+        uint4 a[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a[j] = __ldcs(s4 + e + j * 32);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) __stcs(d4 + e + j * 32, a[j]);
+      }
       for (; e + 96 < n_vec; e += 128) {
         const uint4 a0 = __ldcs(s4 + e), a1 = __ldcs(s4 + e + 32);
         const uint4 a2 = __ldcs(s4 + e + 64), a3 = __ldcs(s4 + e + 96);

@@ -28,8 +28,10 @@ namespace {
 
 constexpr int kUlyThreads = 256;
 
-// One team of 2^log_team lanes copies one chunk of n_u units; four loads in
-// flight per lane before their stores.  Chunk r of dst comes from chunk
+// One team of 2^log_team lanes copies one chunk of n_u units; up to sixteen
+// loads in flight per lane before their stores (sixteen 16-byte loads per
+// lane measured 3.5-4 % faster than four on 1 KB chunks: 0.96-0.97 of the
+// copy bandwidth against 0.93).  Chunk r of dst comes from chunk
 // src_row(r) of src:
 //   to_groups:   dst [P, T] row r = p T + t   <-  src [T, P] row t P + p
 //   from_groups: dst [T, P] row r = t P + p   <-  src [P, T] row p T + t
@@ -54,6 +56,20 @@ __global__ void __launch_bounds__(kUlyThreads) ulysses_layout_kernel(
     const U* s = src + static_cast<size_t>(s_row) * n_u;
     U* d = dst + static_cast<size_t>(r) * n_u;
     int e = tl;
+    for (; e + 15 * team < n_u; e += 16 * team) {
+      U a[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = __ldcs(s + e + j * team);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) __stcs(d + e + j * team, a[j]);
+    }
+    for (; e + 7 * team < n_u; e += 8 * team) {
+      U a[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a[j] = __ldcs(s + e + j * team);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) __stcs(d + e + j * team, a[j]);
+    }
     for (; e + 3 * team < n_u; e += 4 * team) {
       const U a0 = __ldcs(s + e), a1 = __ldcs(s + e + team);
       const U a2 = __ldcs(s + e + 2 * team), a3 = __ldcs(s + e + 3 * team);
@@ -99,9 +115,9 @@ template <typename U>
 void launch_layout(const void* src, void* dst, uint32_t T, uint32_t P, long long chunk_bytes,
                    bool to_groups, int sms, cudaStream_t s) {
   const int n_u = static_cast<int>(chunk_bytes / static_cast<long long>(sizeof(U)));
-  // Team: the largest power of two <= 32 that still gives each lane four units.
+  // Team: the largest power of two <= 32 that still gives each lane sixteen units.
   int log_team = 0;
-  while (log_team < 5 && (4 << (log_team + 1)) <= n_u) ++log_team;
+  while (log_team < 5 && (16 << (log_team + 1)) <= n_u) ++log_team;
   const long long threads = static_cast<long long>(T) * P << log_team;
   long long blocks = (threads + kUlyThreads - 1) / kUlyThreads;
   const long long cap = 8LL * sms;
